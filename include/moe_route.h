@@ -1,0 +1,214 @@
+/*
+ * moe_route.h -- C ABI of the GB300 fused mixture-of-experts layer forward.
+ *
+ * The library computes, for T tokens, E experts and top-k routing:
+ *   a-1  NaN-safe softmax / sigmoid top-k routing with k distinct ids
+ *        (PR #39593 "Fix FlashInfer CUTLASS BF16 + CUDA graphs IMA",
+ *        section "Fix": NaN replaced by -FLT_MAX in-register before scoring
+ *        and before the arg-max; "topK now returns K distinct indices"),
+ *   a-2  count and permute token rows by expert (H20 article, para. 3:
+ *        "the number of rows assigned to each expert"),
+ *   a-3  the tile plan from the rows-per-expert estimate
+ *        est = max(1, ceil(T*k/E)), applied after the worst-case workspace
+ *        capacity is fixed (H20 article, para. 3),
+ *   a-4  grouped gate+up GEMM, a-5 SiLU(gate)*up, a-6 grouped down GEMM,
+ *   a-7  the top-k weighted combine back to token order
+ *        (H20 article, para. 2: fused expert computations with FP8 block
+ *        scaling; Lab notes #6, "Method": fp8_w8a8, block [128,128]).
+ *
+ * Conventions for every call:
+ *  - Every pointer argument named "device" is a device pointer the caller
+ *    owns (e.g. from torch); the library never allocates device memory and
+ *    keeps no state beyond a per-device cache of kernel attributes.
+ *  - `stream` is a cudaStream_t passed as void*; all device work is
+ *    enqueued on it asynchronously.  No call below synchronises, except
+ *    moe_check.
+ *  - Every call returns MOE_OK (0) or a negative MOE_ERR_* code.  Argument
+ *    and shape validation happens before any launch; nothing is enqueued
+ *    when an argument is rejected.
+ *  - Layouts are row-major (C order).  "flat index" f = t*k + j, where j is
+ *    the rank of the pick within token t (0 = highest scored).
+ *
+ * Weights:  w13 [E, 2I, H]: rows [0, I) are the gate projection and rows
+ *           [I, 2I) the up projection of each expert; w2 [E, H, I].
+ *  MOE_DTYPE_F32:  x [T,H] f32, logits [T,E] f32, w13/w2 f32, out [T,H]
+ *                  f32.  GEMMs run on the tensor cores as TF32.
+ *  MOE_DTYPE_BF16: x, logits, w13, w2 and out in bf16.
+ *  MOE_DTYPE_FP8_BLOCK128: x and logits bf16; w13 / w2 are e4m3 codes with
+ *                  fp32 block scales s13 [E, 2I/128, H/128] and
+ *                  s2 [E, H/128, I/128] (one scale per [128,128] block);
+ *                  activations are quantised inside the call per token and
+ *                  128-column group (scale = max(amax,1e-10)/448, clamp
+ *                  fmaxf(fminf(v,448),-448), round to nearest even);
+ *                  out bf16.
+ */
+#ifndef MOE_ROUTE_H
+#define MOE_ROUTE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+/* return codes */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1) /* null pointer, bad size, bad enum, misaligned pointer */
+#define MOE_ERR_UNSUPPORTED (-2) /* valid but not supported (e.g. FP8 with H % 128 != 0) */
+#define MOE_ERR_WORKSPACE (-3)   /* ws_bytes smaller than plan->workspace_bytes */
+#define MOE_ERR_CUDA (-4)        /* a CUDA runtime call or launch failed */
+#define MOE_ERR_DEVICE (-5)      /* moe_check: the device error word is set */
+#define MOE_ERR_TIMEOUT (-6)     /* moe_check: a device wait gave up */
+
+/* device error word bits (moe_check) */
+#define MOE_DEVERR_BAD_ID 1u   /* a caller-supplied id outside [0, E) (skipped) */
+#define MOE_DEVERR_DUP_ID 2u   /* a caller-supplied id repeated within a token (skipped) */
+#define MOE_DEVERR_TIMEOUT 4u  /* a pipeline wait exceeded its limit; kernel returned */
+#define MOE_DEVERR_CAPACITY 8u /* tile list would exceed the planned capacity */
+
+/* compute dtypes */
+#define MOE_DTYPE_F32 0
+#define MOE_DTYPE_BF16 1
+#define MOE_DTYPE_FP8_BLOCK128 2
+
+/* logits dtypes (moe_route_topk) */
+#define MOE_LOGITS_F32 0
+#define MOE_LOGITS_BF16 1
+
+/* scoring */
+#define MOE_SCORING_SOFTMAX 0
+#define MOE_SCORING_SIGMOID 1
+
+/*
+ * The plan: pure host arithmetic, filled by moe_plan.  All offsets are
+ * byte offsets into the caller's workspace, 256-byte aligned, so that tests
+ * can read the intermediates:
+ *   ids     int32 [T, k]    chosen expert per pick (-1 = skipped, see with_ids)
+ *   w       f32   [T, k]    combine weight per pick
+ *   counts  int32 [E]       rows per expert
+ *   offsets int32 [E + 1]   exclusive scan of counts
+ *   src     int32 [T*k]     permuted row -> flat index (expert-major,
+ *                           ascending flat index within an expert)
+ *   pos     int32 [T*k]     flat index -> permuted row (inverse of src)
+ *   tiles   int32 [max_tiles, 4]  {expert, first row, rows, 0} token tiles
+ *   ntiles  int32 [1]       number of valid tiles
+ *   err     uint32 [1]      device error word (MOE_DEVERR_* bits)
+ * The remaining regions (chunk counts, permuted activations, scales, the
+ * fp32 combine accumulator) are internal.
+ */
+typedef struct moe_plan {
+  int32_t abi_version;
+  int32_t T, H, I, E, k;
+  int32_t dtype, scoring, renorm;
+  int32_t est;        /* rows-per-expert estimate used for the tile choice */
+  int32_t force_est;  /* 0, or the caller's override (e.g. T: old estimate) */
+  int32_t tile_n;     /* token tile = MMA N (16, 32, 64 or 128) */
+  int32_t route_tpc;  /* tokens per routing CTA */
+  int32_t n_chunks;   /* routing CTAs = ceil(T / route_tpc) */
+  int32_t max_tiles;  /* worst-case token tiles (independent of est) */
+  int32_t g1_mblocks; /* ceil(I / 128) gate+up feature blocks */
+  int32_t g2_mblocks; /* ceil(H / 128) output feature blocks */
+  int32_t reserved0;
+  uint64_t workspace_bytes;
+  uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
+  uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;
+  uint64_t off_xq, off_xs, off_act, off_as, off_acc;
+  uint64_t reserved1[4];
+} moe_plan_t;
+
+/*
+ * moe_plan -- fill *plan for one layer shape.  Pure host arithmetic; no
+ * device call.  Requirements: T >= 0; 1 <= E <= 1024; 1 <= k <= min(E, 32);
+ * H, I multiples of 32 (F32), 64 (BF16) or 128 (FP8); scoring softmax or
+ * sigmoid.  The workspace capacity is fixed first from (T, k, E, H, I,
+ * dtype) alone; then est = force_est if force_est > 0, else
+ * max(1, ceil(T*k/E)), and tile_n = 16 / 32 / 64 / 128 for est <= 16 /
+ * <= 32 / <= 64 / above.
+ * Errors: MOE_ERR_INVALID_ARG (null plan, negative or out-of-range sizes,
+ * bad enums), MOE_ERR_UNSUPPORTED (H or I not a multiple of the dtype's
+ * K step).
+ */
+int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm, int force_est,
+             moe_plan_t* plan);
+
+/*
+ * moe_forward -- steps a-1 .. a-7 for one batch, asynchronously on stream.
+ *   x       device, [T, H] (f32 for F32, else bf16)
+ *   logits  device, [T, E] gating logits (f32 for F32, else bf16); NaN and
+ *           +-Inf allowed (NaN -> -FLT_MAX, +-Inf -> +-FLT_MAX)
+ *   w13     device, [E, 2I, H]; w2 device, [E, H, I] (dtype per plan)
+ *   s13,s2  device fp32 block scales for FP8, else must be NULL
+ *   out     device, [T, H] (f32 for F32, else bf16); fully overwritten
+ *   ws      device workspace of ws_bytes >= plan->workspace_bytes
+ * x, w13, w2, out and ws must be 16-byte aligned.  T == 0 enqueues nothing
+ * and accepts null activation, output and workspace pointers.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_WORKSPACE, MOE_ERR_CUDA.
+ */
+int moe_forward(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
+                const float* s13, const void* w2, const float* s2, void* out, void* ws,
+                size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward_timed -- moe_forward that also records caller-created CUDA
+ * events (cudaEvent_t passed as void*) on `stream` at the boundaries of its
+ * launches, for per-kernel timing without a profiler: events[0] before the
+ * routing kernel, [1] after routing, [2] after the scan, [3] after the
+ * gather, [4] after grouped GEMM 1, [5] after grouped GEMM 2, [6] after the
+ * output cast ([6] directly follows [5] for f32 layers).  n_events must be
+ * 7.  Same arguments, errors and results as moe_forward otherwise.
+ */
+int moe_forward_timed(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
+                      const float* s13, const void* w2, const float* s2, void* out, void* ws,
+                      size_t ws_bytes, void* stream, void* const* events, int n_events);
+
+/*
+ * moe_forward_with_ids -- as moe_forward, but routing (a-1) is replaced by
+ * caller-supplied ids (device int32 [T, k]) and weights (device f32
+ * [T, k]).  Each pick is validated on the device: an id outside [0, E), or
+ * repeated within its token, sets MOE_DEVERR_BAD_ID / MOE_DEVERR_DUP_ID in
+ * the error word and that pick is skipped (contributes nothing) instead of
+ * being used as an index.  This is the fault-test entry for the
+ * duplicate-id failure described in PR #39593 ("Root cause").
+ */
+int moe_forward_with_ids(const moe_plan_t* plan, const void* x, const int32_t* ids,
+                         const float* topk_w, const void* w13, const float* s13, const void* w2,
+                         const float* s2, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_route_topk -- step a-1 alone: logits (device [T, E], MOE_LOGITS_*)
+ * -> ids (device int32 [T, k]) and w (device f32 [T, k]).  Selection is on
+ * the sanitised logits, descending, ties to the lower expert index; softmax
+ * weights are exp(l - max) / sum over all E, sigmoid weights 1/(1+exp(-l));
+ * renorm != 0 rescales the k weights to sum to one (1/k each when their sum
+ * is zero or not finite).  Requires 1 <= E <= 1024, 1 <= k <= min(E, 32).
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.
+ */
+int moe_route_topk(const void* logits, int logits_dtype, int T, int E, int k, int scoring,
+                   int renorm, int32_t* ids, float* w, void* stream);
+
+/*
+ * moe_check -- synchronise `stream`, read the workspace error word, clear
+ * it, and return MOE_OK, MOE_ERR_TIMEOUT (timeout bit set) or
+ * MOE_ERR_DEVICE (any other bit).  *bits (if not NULL) receives the word.
+ */
+int moe_check(const moe_plan_t* plan, void* ws, uint32_t* bits, void* stream);
+
+/* moe_plan_describe -- a one-line text summary of the plan (est, tile,
+ * workspace) into buf (NUL-terminated, truncated to n).  Returns the
+ * length it wanted, or MOE_ERR_INVALID_ARG. */
+int moe_plan_describe(const moe_plan_t* plan, char* buf, size_t n);
+
+/* moe_strerror -- static message for a MOE_* return code. */
+const char* moe_strerror(int code);
+
+/* moe_abi_version -- MOE_ABI_VERSION of the built library. */
+int moe_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_ROUTE_H */

@@ -1,0 +1,455 @@
+// grouped_gemm.cu -- tcgen05/TMEM grouped GEMMs of the fused MoE layer
+// (steps a-4 .. a-7), fed by TMA, for TF32, BF16 and block-scaled FP8 e4m3.
+//
+// One persistent CTA per SM walks a device-built list of work items
+// (token tile x 128-row weight block).  Swap-AB orientation: the MMA's M
+// side is 128 rows of one expert's weight matrix, its N side a tile of
+// `N` permuted token rows of that expert (N = 16 .. 128 chosen from the
+// rows-per-expert estimate, H20 article para. 3), so a decode-sized expert
+// with a handful of rows still fills the 128-wide M side with weights.
+//
+//   warp 0      TMA producer: weight tile(s) + token tile per 128-byte K step
+//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//   warps 2..9  epilogue: tcgen05.ld from TMEM, then
+//                 G1: act = SiLU(gate) * up  (FP8: + per-token 128-group
+//                     e4m3 quantisation, clamp with fminf/fmaxf as in
+//                     PR #39593 "Purpose")
+//                 G2: out_acc[t] += w[t,j] * y  (the top-k weighted combine)
+//
+// FP8 [128,128] block scales (Lab notes #6, config file line): each 128-K
+// block is accumulated into its own TMEM buffer (double-buffered) and the
+// epilogue warps fold it into fp32 registers with weight-scale x
+// activation-scale, so arbitrary fp32 scales are honoured exactly.
+//
+// Every wait is bounded (see mbar_wait); a timeout sets MOE_DEVERR_TIMEOUT
+// in the error word, raises a CTA-wide abort flag, drains in-flight copies
+// and MMAs, frees TMEM and returns.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "moe_internal.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+
+constexpr int kThreads = 320;
+constexpr int kEpiThreads = 256;
+constexpr int kMaxHalf = 64;  // columns per epilogue thread at tile_n = 128
+constexpr unsigned kDevErrTimeout = 4u;
+
+template <int KIND>
+struct KindTraits;
+template <>
+struct KindTraits<KIND_TF32> {
+  static constexpr uint32_t fmt = 2;
+  static constexpr int esize = 4;
+};
+template <>
+struct KindTraits<KIND_BF16> {
+  static constexpr uint32_t fmt = 1;
+  static constexpr int esize = 2;
+};
+template <>
+struct KindTraits<KIND_E4M3> {
+  static constexpr uint32_t fmt = 0;
+  static constexpr int esize = 1;
+};
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
+
+template <int KIND>
+__device__ __forceinline__ void store_act(void* act, size_t idx, float v);
+template <>
+__device__ __forceinline__ void store_act<KIND_TF32>(void* act, size_t idx, float v) {
+  static_cast<float*>(act)[idx] = v;
+}
+template <>
+__device__ __forceinline__ void store_act<KIND_BF16>(void* act, size_t idx, float v) {
+  static_cast<__nv_bfloat16*>(act)[idx] = __float2bfloat16_rn(v);
+}
+
+template <int KIND, int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
+                        const __grid_constant__ CUtensorMap tma_b, const GemmArgs args) {
+  constexpr int NA = (G == 1) ? 2 : 1;  // G1 multiplies gate and up tiles
+  constexpr bool FP8 = (KIND == KIND_E4M3);
+  constexpr int BKE = 128 / KindTraits<KIND>::esize;  // elements per 128-byte K step
+  extern __shared__ uint8_t smem_raw[];
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int N = args.N;
+  const int S = args.stages;
+  const uint32_t stage_bytes = NA * 16384u + static_cast<uint32_t>(N) * 128u;
+  const uint64_t limit = args.limit_ns;
+
+  // ---- shared memory carve-up (stage ring 1024-aligned for 128B swizzle)
+  uint8_t* stages = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + static_cast<size_t>(S) * stage_bytes);
+  uint64_t* empty = full + S;
+  uint64_t* accf = empty + S;  // [2] accumulator (or FP8 partial) ready
+  uint64_t* acce = accf + 2;   // [2] accumulator drained by the epilogue
+  uint64_t* done = acce + 2;   // all MMAs of this CTA complete
+  uint64_t* epib = done + 1;   // epilogue-internal barrier
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epib + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);  // [N][kblocks]
+  float* red = sb + N * args.kblocks;                                             // [4][N]
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&accf[b]), 1);
+      mbar_init(smem_u32(&acce[b]), kEpiThreads);
+    }
+    mbar_init(smem_u32(done), 1);
+    mbar_init(smem_u32(epib), kEpiThreads);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tma_a);
+    prefetch_tmap(&tma_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int nwork = (*args.ntiles) * args.mblocks;
+  int never = 0;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_w = policy_evict_first();  // weights: streamed once
+      const uint64_t pol_x = policy_evict_last();   // token tiles: reused per block
+      uint32_t it = 0;
+      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+        const int4 tile = args.tiles[w / args.mblocks];
+        const int mb = w % args.mblocks;
+        const int a_row = tile.x * args.a_rows_per_e + mb * 128;
+        for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
+          const int s = static_cast<int>(it % S);
+          if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1u) ^ 1u, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = stages + static_cast<size_t>(s) * stage_bytes;
+          const uint32_t fb = smem_u32(&full[s]);
+          mbar_arrive_expect_tx(fb, stage_bytes);
+          const int kx = kb * BKE;
+          tma_load_2d(smem_u32(st), &tma_a, fb, kx, a_row, pol_w);
+          if (NA == 2) tma_load_2d(smem_u32(st + 16384), &tma_a, fb, kx, a_row + args.a_up_off, pol_w);
+          tma_load_2d(smem_u32(st + NA * 16384), &tma_b, fb, kx, tile.y, pol_x);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(args.err, kDevErrTimeout);
+      }
+      // never leave with copies in flight: wait for the last S stages issued
+      for (uint32_t j = (it > static_cast<uint32_t>(S) ? it - S : 0u); j < it; ++j)
+        mbar_wait(smem_u32(&full[j % S]), (j / S) & 1u, limit, &never);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(N));
+      uint32_t it = 0, tc = 0, kc = 0;
+      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+        uint32_t dbase = 0;
+        if (!FP8) {
+          const uint32_t buf = tc & 1u;
+          if (!mbar_wait(smem_u32(&acce[buf]), ((tc >> 1) & 1u) ^ 1u, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          dbase = buf * NA * N;
+        }
+        for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
+          const int s = static_cast<int>(it % S);
+          if (!mbar_wait(smem_u32(&full[s]), (it / S) & 1u, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t pb = 0;
+          if (FP8) {
+            pb = kc & 1u;
+            if (!mbar_wait(smem_u32(&acce[pb]), ((kc >> 1) & 1u) ^ 1u, limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            dbase = pb * NA * N;
+          }
+          const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * stage_bytes);
+#pragma unroll
+          for (int a = 0; a < NA; ++a) {
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = sdesc_sw128(sa + a * 16384 + ks * 32);
+              const uint64_t bd = sdesc_sw128(sa + NA * 16384 + ks * 32);
+              const uint32_t accumulate = FP8 ? (ks != 0) : ((kb | ks) != 0);
+              mma_issue<KIND>(tmem_base + dbase + a * N, ad, bd, idesc, accumulate);
+            }
+          }
+          mma_commit(smem_u32(&empty[s]));  // frees the stage once read
+          if (FP8) {
+            mma_commit(smem_u32(&accf[pb]));
+            ++kc;
+          }
+        }
+        if (!ok) break;
+        if (!FP8) {
+          mma_commit(smem_u32(&accf[tc & 1u]));
+          ++tc;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        atomicOr(args.err, kDevErrTimeout);
+      }
+      // never free TMEM under a running MMA
+      mma_commit(smem_u32(done));
+      mbar_wait(smem_u32(done), 0, limit, &never);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int ew = warp - 2;
+    const int q = warp & 3;     // TMEM lane quadrant this warp may read
+    const int half = ew >> 2;   // which half of the token columns
+    const int hc = N >> 1;      // columns per thread
+    const int c_begin = half * hc;
+    const int r_in_tile = q * 32 + lane;
+    const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
+    uint32_t tc = 0, kc = 0, eb = 0;
+
+    auto ep_barrier = [&]() -> bool {
+      mbar_arrive(smem_u32(epib));
+      const bool got = mbar_wait(smem_u32(epib), eb & 1u, limit, abort_flag);
+      ++eb;
+      return __all_sync(0xffffffffu, got);
+    };
+
+    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+      const int4 tile = args.tiles[w / args.mblocks];
+      const int mb = w % args.mblocks;
+      const int row0 = tile.y, nrows = tile.z;
+      const int row = mb * 128 + r_in_tile;  // weight row = output feature
+      const bool row_ok = row < args.m_valid;
+
+      if constexpr (!FP8) {
+        const uint32_t buf = tc & 1u;
+        const bool got = mbar_wait(smem_u32(&accf[buf]), (tc >> 1) & 1u, limit, abort_flag);
+        if (!__all_sync(0xffffffffu, got)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dcol = buf * NA * N;
+        for (int c0 = 0; c0 < hc; c0 += 8) {
+          const int cc = c_begin + c0;
+          if constexpr (G == 1) {
+            float gv[8], uv[8];
+            tmem_ld8(lane_addr + dcol + cc, gv);
+            tmem_ld8(lane_addr + dcol + N + cc, uv);
+            tmem_wait_ld(gv, uv);
+            if (row_ok) {
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int j = cc + jj;
+                if (j < nrows)
+                  store_act<KIND>(args.act, static_cast<size_t>(row0 + j) * args.I + row,
+                                  silu_f(gv[jj]) * uv[jj]);
+              }
+            }
+          } else {
+            float yv[8];
+            tmem_ld8(lane_addr + dcol + cc, yv);
+            tmem_wait_ld(yv);
+            if (row_ok) {
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const int j = cc + jj;
+                if (j < nrows) {
+                  const int f = __ldg(args.src + row0 + j);
+                  const int t = f / args.k;
+                  atomicAdd(args.out_acc + static_cast<size_t>(t) * args.H + row,
+                            __ldg(args.topw + f) * yv[jj]);
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(smem_u32(&acce[buf]));
+        ++tc;
+      } else {
+        // -------- FP8: stage this tile's activation scales [N][kblocks]
+        const int kbs = args.kblocks;
+        if (!ep_barrier()) {
+          ok = false;
+          break;
+        }
+        for (int i = ew * 32 + lane; i < N * kbs; i += kEpiThreads) {
+          const int j = i / kbs;
+          sb[i] = (j < nrows) ? __ldg(args.b_scale + static_cast<size_t>(row0 + j) * kbs + (i % kbs))
+                              : 0.0f;
+        }
+        if (!ep_barrier()) {
+          ok = false;
+          break;
+        }
+        float acc0[kMaxHalf], acc1[kMaxHalf];  // acc1 (up) is dead code for G2
+#pragma unroll
+        for (int c = 0; c < kMaxHalf; ++c) {
+          acc0[c] = 0.0f;
+          acc1[c] = 0.0f;
+        }
+        const float* sw0 =
+            args.w_scale + (static_cast<size_t>(tile.x) * args.w_scale_rows_per_e + mb) * kbs;
+        const float* sw1 = sw0 + static_cast<size_t>(args.I / 128) * kbs;  // up rows (G1)
+        for (int kb = 0; kb < kbs; ++kb, ++kc) {
+          const uint32_t pb = kc & 1u;
+          const bool got = mbar_wait(smem_u32(&accf[pb]), (kc >> 1) & 1u, limit, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float s0 = __ldg(sw0 + kb);
+          const float s1 = (NA == 2) ? __ldg(sw1 + kb) : 0.0f;
+          const uint32_t dcol = pb * NA * N;
+#pragma unroll
+          for (int c0 = 0; c0 < kMaxHalf; c0 += 8) {
+            if (c0 < hc) {
+              const int cc = c_begin + c0;
+              float p0[8], p1[8];
+              tmem_ld8(lane_addr + dcol + cc, p0);
+              if (NA == 2) {
+                tmem_ld8(lane_addr + dcol + N + cc, p1);
+                tmem_wait_ld(p0, p1);
+              } else {
+                tmem_wait_ld(p0);
+              }
+#pragma unroll
+              for (int jj = 0; jj < 8; ++jj) {
+                const float bs = sb[(cc + jj) * kbs + kb];
+                acc0[c0 + jj] = fmaf(p0[jj], s0 * bs, acc0[c0 + jj]);
+                if (NA == 2) acc1[c0 + jj] = fmaf(p1[jj], s1 * bs, acc1[c0 + jj]);
+              }
+            }
+          }
+          tc_fence_before();
+          mbar_arrive(smem_u32(&acce[pb]));
+        }
+        if (!ok) break;
+
+        if constexpr (G == 1) {
+          // act = SiLU(gate) * up, then e4m3 per token over this 128-row group
+#pragma unroll
+          for (int c = 0; c < kMaxHalf; ++c) {
+            if (c < hc) {
+              acc0[c] = silu_f(acc0[c]) * acc1[c];
+              float m = fabsf(acc0[c]);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+              if (lane == 0) red[q * N + c_begin + c] = m;
+            }
+          }
+          if (!ep_barrier()) {
+            ok = false;
+            break;
+          }
+          uint8_t* act_q = static_cast<uint8_t*>(args.act);
+          const int groups = args.I / 128;
+#pragma unroll
+          for (int c = 0; c < kMaxHalf; ++c) {
+            if (c < hc) {
+              const int j = c_begin + c;
+              if (j < nrows) {
+                const float amax =
+                    fmaxf(fmaxf(red[j], red[N + j]), fmaxf(red[2 * N + j], red[3 * N + j]));
+                const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+                float v = __fdiv_rn(acc0[c], scale);
+                v = fmaxf(fminf(v, 448.0f), -448.0f);
+                const size_t slot = static_cast<size_t>(row0 + j);
+                act_q[slot * args.I + row] = static_cast<uint8_t>(
+                    __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+                if (r_in_tile == 0) args.act_scale[slot * groups + mb] = scale;
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kMaxHalf; ++c) {
+            if (c < hc) {
+              const int j = c_begin + c;
+              if (j < nrows && row_ok) {
+                const int f = __ldg(args.src + row0 + j);
+                const int t = f / args.k;
+                atomicAdd(args.out_acc + static_cast<size_t>(t) * args.H + row,
+                          __ldg(args.topw + f) * acc0[c]);
+              }
+            }
+          }
+        }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      if (lane == 0) atomicOr(args.err, kDevErrTimeout);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem_base, args.tmem_cols);
+}
+
+template <int KIND, int G>
+static cudaError_t launch_one(const GemmArgs& args, const CUtensorMap& ta, const CUtensorMap& tb,
+                              int grid, int smem, cudaStream_t stream) {
+  auto kern = grouped_gemm_kernel<KIND, G>;
+  static int configured = 0;  // max dynamic smem is a per-function attribute
+  if (configured < smem) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured = smem;
+  }
+  kern<<<grid, kThreads, smem, stream>>>(ta, tb, args);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const CUtensorMap& ta,
+                                const CUtensorMap& tb, int grid, int smem, cudaStream_t stream) {
+  if (kind == KIND_TF32) {
+    return g == 1 ? launch_one<KIND_TF32, 1>(args, ta, tb, grid, smem, stream)
+                  : launch_one<KIND_TF32, 2>(args, ta, tb, grid, smem, stream);
+  }
+  if (kind == KIND_BF16) {
+    return g == 1 ? launch_one<KIND_BF16, 1>(args, ta, tb, grid, smem, stream)
+                  : launch_one<KIND_BF16, 2>(args, ta, tb, grid, smem, stream);
+  }
+  return g == 1 ? launch_one<KIND_E4M3, 1>(args, ta, tb, grid, smem, stream)
+                : launch_one<KIND_E4M3, 2>(args, ta, tb, grid, smem, stream);
+}
+
+}  // namespace moe

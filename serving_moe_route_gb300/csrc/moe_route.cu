@@ -1,0 +1,745 @@
+// moe_route.cu -- host C ABI (include/moe_route.h) and the routing,
+// permutation, gather and output kernels of the fused MoE layer forward.
+//
+// Launch sequence of moe_forward on the caller's stream:
+//   route_kernel    a-1 routing (warp per token, NaN -> -FLT_MAX in
+//                   registers, k rounds of warp arg-max with ties to the
+//                   lower expert index) + per-CTA expert histogram and the
+//                   rank of each pick among equal ids in its CTA
+//   scan_kernel     a-2/a-3: per-expert totals, exclusive scans, per-CTA
+//                   bases and the token-tile work list (single CTA)
+//   gather_kernel   a-2: slot of every pick, src/pos, permuted activation
+//                   rows (FP8: quantised per 128-column group), zeroes the
+//                   fp32 combine accumulator
+//   grouped GEMM 1  a-4/a-5 (grouped_gemm.cu)
+//   grouped GEMM 2  a-6/a-7 (grouped_gemm.cu)
+//   cast_kernel     fp32 accumulator -> bf16 output (not for f32 layers)
+// No atomics are used to count or place rows: every slot follows from
+// counts and ranks computed without them.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/moe_route.h"
+#include "moe_internal.cuh"
+
+namespace moe {
+
+constexpr int kRouteThreads = 256;  // 8 warps
+constexpr int kMaxK = 32;
+constexpr int kMaxE = 1024;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+
+// ------------------------------------------------------------------ routing
+__device__ __forceinline__ float sanitize_logit(float v) {
+  // NaN -> -FLT_MAX (PR #39593, "Fix"); +-Inf -> +-FLT_MAX so weights stay finite
+  if (isnan(v)) return -FLT_MAX;
+  if (isinf(v)) return v > 0.0f ? FLT_MAX : -FLT_MAX;
+  return v;
+}
+
+__device__ __forceinline__ float load_logit(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float load_logit(const __nv_bfloat16* p) {
+  return __bfloat162float(p[0]);
+}
+
+// mode 0: routing only; 1: routing + histogram; 2: validate caller ids + histogram
+template <int VPT, typename LT>
+__global__ void __launch_bounds__(kRouteThreads)
+    route_kernel(const LT* __restrict__ logits, int T, int E, int k, int scoring, int renorm,
+                 int tpc, int mode, const int* __restrict__ ids_in, const float* __restrict__ w_in,
+                 int* __restrict__ ids, float* __restrict__ w, int* __restrict__ chunk_counts,
+                 int* __restrict__ lrank, unsigned* __restrict__ err) {
+  extern __shared__ int sid[];  // [tpc * k] picks of this CTA's tokens
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * tpc;
+  const int ntok = min(tpc, T - t0);
+
+  for (int tl = warp; tl < ntok; tl += kRouteThreads / 32) {
+    const int t = t0 + tl;
+    int my_id = -1;
+    float my_w = 0.0f;
+    if (mode != 2) {
+      float v[VPT];
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int e = i * 32 + lane;
+        v[i] = (e < E) ? sanitize_logit(load_logit(logits + static_cast<size_t>(t) * E + e)) : 0.0f;
+      }
+      uint32_t taken = 0;
+      float my_v = 0.0f;
+      for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int e = i * 32 + lane;
+          // lane-local experts ascend with i, so '>' keeps the lower index on ties
+          if (e < E && !((taken >> i) & 1u) && v[i] > bv) {
+            bv = v[i];
+            bi = e;
+          }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+          if (ov > bv || (ov == bv && oi < bi)) {
+            bv = ov;
+            bi = oi;
+          }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == j) {
+          my_id = bi;
+          my_v = bv;
+        }
+      }
+      // weights
+      const float vmax = __shfl_sync(0xffffffffu, my_v, 0);  // pick 0 is the row maximum
+      float score = 0.0f;
+      if (scoring == 0) {
+        if (renorm) {
+          score = (lane < k) ? expf(my_v - vmax) : 0.0f;  // the full-row sum cancels
+        } else {
+          float z = 0.0f;
+#pragma unroll
+          for (int i = 0; i < VPT; ++i)
+            if (i * 32 + lane < E) z += expf(v[i] - vmax);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+          score = (lane < k) ? expf(my_v - vmax) / z : 0.0f;
+        }
+      } else {
+        score = (lane < k) ? 1.0f / (1.0f + expf(-my_v)) : 0.0f;
+      }
+      if (renorm) {
+        float den = score;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+        my_w = (den > 0.0f && isfinite(den)) ? score / den : 1.0f / static_cast<float>(k);
+      } else {
+        my_w = score;
+      }
+    } else {
+      // caller-supplied picks: an id outside [0, E) or repeated within the
+      // token is reported and skipped rather than used as an index
+      int id = (lane < k) ? ids_in[static_cast<size_t>(t) * k + lane] : -1;
+      const float wt = (lane < k) ? w_in[static_cast<size_t>(t) * k + lane] : 0.0f;
+      unsigned bad = 0;
+      if (lane < k && (id < 0 || id >= E)) {
+        bad |= 1u;
+        id = -1;
+      }
+      for (int j = 0; j < kMaxK; ++j) {
+        const int other = __shfl_sync(0xffffffffu, id, j);
+        if (j < lane && lane < k && id >= 0 && other == id) {
+          bad |= 2u;
+          id = -1;
+        }
+      }
+      if (bad) atomicOr(err, bad);
+      my_id = id;
+      my_w = wt;
+    }
+    if (lane < k) {
+      ids[static_cast<size_t>(t) * k + lane] = my_id;
+      w[static_cast<size_t>(t) * k + lane] = my_w;
+      if (mode != 0) sid[tl * k + lane] = my_id;
+    }
+  }
+  if (mode == 0) return;
+  __syncthreads();
+
+  // histogram of this CTA's picks and each pick's rank among equal ids
+  const int n = ntok * k;
+  for (int f = threadIdx.x; f < n; f += kRouteThreads) {
+    const int e = sid[f];
+    int r = 0;
+    for (int g = 0; g < f; ++g) r += (sid[g] == e);
+    lrank[static_cast<size_t>(t0) * k + f] = (e >= 0) ? r : -1;
+  }
+  for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+    int c = 0;
+    for (int f = 0; f < n; ++f) c += (sid[f] == e);
+    chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = c;
+  }
+}
+
+// ------------------------------------------------------------------ scan
+// Block-wide exclusive scan of one int per thread (blockDim = 1024).
+__device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int s = warp_sums[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, s, off);
+      if (lane >= off) s += y;
+    }
+    warp_sums[lane] = s;  // inclusive
+    if (lane == 31) *total = s;
+  }
+  __syncthreads();
+  const int before = (warp > 0 ? warp_sums[warp - 1] : 0) + x - v;
+  __syncthreads();
+  return before;
+}
+
+__global__ void __launch_bounds__(1024)
+    scan_kernel(const int* __restrict__ chunk_counts, int n_chunks, int E, int tile_n,
+                int max_tiles, int* __restrict__ chunk_base, int* __restrict__ counts,
+                int* __restrict__ offsets, int4* __restrict__ tiles, int* __restrict__ ntiles,
+                unsigned* __restrict__ err) {
+  __shared__ int warp_sums[32];
+  __shared__ int tot_rows, tot_tiles;
+  const int e = threadIdx.x;
+  int cnt = 0;
+  if (e < E) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const size_t i = static_cast<size_t>(c) * E + e;
+      chunk_base[i] = cnt;
+      cnt += chunk_counts[i];
+    }
+    counts[e] = cnt;
+  }
+  const int ntl = (cnt + tile_n - 1) / tile_n;
+  const int off = block_exclusive_scan(cnt, warp_sums, &tot_rows);
+  const int tstart = block_exclusive_scan(ntl, warp_sums, &tot_tiles);
+  if (e < E) offsets[e] = off;
+  if (e == 0) {
+    offsets[E] = tot_rows;
+    const int nt = min(tot_tiles, max_tiles);
+    if (tot_tiles > max_tiles) atomicOr(err, 8u);
+    *ntiles = nt;
+  }
+  if (e < E) {
+    for (int i = 0; i < ntl && tstart + i < max_tiles; ++i)
+      tiles[tstart + i] = make_int4(e, off + i * tile_n, min(tile_n, cnt - i * tile_n), 0);
+  }
+}
+
+// ------------------------------------------------------------------ gather
+// One warp per pick f: its slot, src/pos, and the permuted activation row.
+// XT: input element type; QT: 0 copy f32, 1 copy bf16, 2 quantise bf16 -> e4m3
+template <int QT>
+__global__ void __launch_bounds__(256)
+    gather_kernel(const void* __restrict__ x, const int* __restrict__ ids,
+                  const int* __restrict__ lrank, const int* __restrict__ chunk_base,
+                  const int* __restrict__ offsets, int T, int H, int E, int k, int tpc,
+                  int* __restrict__ src, int* __restrict__ pos, void* __restrict__ xq,
+                  float* __restrict__ xs, float* __restrict__ acc, long long acc_elems) {
+  const int lane = threadIdx.x & 31;
+  const long long R = static_cast<long long>(T) * k;
+  const long long f = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+
+  // zero the fp32 combine accumulator (grid-stride, float4)
+  {
+    float4* a4 = reinterpret_cast<float4*>(acc);
+    const long long n4 = acc_elems >> 2;
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+         i += stride)
+      a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  if (f >= R) return;
+  const int e = ids[f];
+  if (e < 0) {
+    if (lane == 0) pos[f] = -1;
+    return;
+  }
+  const int t = static_cast<int>(f / k);
+  const int c = t / tpc;
+  const int slot = offsets[e] + chunk_base[static_cast<size_t>(c) * E + e] + lrank[f];
+  if (lane == 0) {
+    src[slot] = static_cast<int>(f);
+    pos[f] = slot;
+  }
+  if constexpr (QT == 0) {
+    const float4* xr = reinterpret_cast<const float4*>(static_cast<const float*>(x) +
+                                                       static_cast<size_t>(t) * H);
+    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(xq) + static_cast<size_t>(slot) * H);
+    for (int i = lane; i < H / 4; i += 32) dst[i] = __ldg(xr + i);
+  } else if constexpr (QT == 1) {
+    const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) +
+                                                     static_cast<size_t>(t) * H);
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(xq) +
+                                          static_cast<size_t>(slot) * H);
+    for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(xr + i);
+  } else {
+    // per 128-column group: 4 values per lane
+    const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(x) + static_cast<size_t>(t) * H;
+    uint8_t* dst = static_cast<uint8_t*>(xq) + static_cast<size_t>(slot) * H;
+    const int groups = H / 128;
+    for (int g = 0; g < groups; ++g) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + g * 128 + lane * 4));
+      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
+      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
+      float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
+      float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      const float scale = __fdiv_rn(fmaxf(m, 1e-10f), 448.0f);
+      uint32_t packed = 0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        float q = __fdiv_rn(v[i], scale);
+        q = fmaxf(fminf(q, 448.0f), -448.0f);
+        packed |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3))
+                  << (8 * i);
+      }
+      *reinterpret_cast<uint32_t*>(dst + g * 128 + lane * 4) = packed;
+      if (lane == 0) xs[static_cast<size_t>(slot) * groups + g] = scale;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ output
+__global__ void __launch_bounds__(256)
+    cast_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out, long long n) {
+  const long long n4 = n >> 2;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
+       i += stride) {
+    const float4 v = reinterpret_cast<const float4*>(acc)[i];
+    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+    uint2 o;
+    o.x = *reinterpret_cast<uint32_t*>(&a);
+    o.y = *reinterpret_cast<uint32_t*>(&b);
+    reinterpret_cast<uint2*>(out)[i] = o;
+  }
+}
+
+// ------------------------------------------------------------------ host helpers
+static int vpt_for(int E) {
+  const int v = (E + 31) / 32;
+  if (v <= 1) return 1;
+  if (v <= 2) return 2;
+  if (v <= 4) return 4;
+  if (v <= 8) return 8;
+  if (v <= 16) return 16;
+  return 32;
+}
+
+template <typename LT>
+static void launch_route_t(int vpt, dim3 grid, size_t smem, cudaStream_t st, const LT* logits,
+                           int T, int E, int k, int scoring, int renorm, int tpc, int mode,
+                           const int* ids_in, const float* w_in, int* ids, float* w, int* cc,
+                           int* lr, unsigned* err) {
+#define MOE_ROUTE_CASE(V)                                                                      \
+  case V:                                                                                      \
+    route_kernel<V, LT><<<grid, kRouteThreads, smem, st>>>(logits, T, E, k, scoring, renorm, \
+                                                           tpc, mode, ids_in, w_in, ids, w,  \
+                                                           cc, lr, err);                     \
+    break;
+  switch (vpt) {
+    MOE_ROUTE_CASE(1)
+    MOE_ROUTE_CASE(2)
+    MOE_ROUTE_CASE(4)
+    MOE_ROUTE_CASE(8)
+    MOE_ROUTE_CASE(16)
+    MOE_ROUTE_CASE(32)
+  }
+#undef MOE_ROUTE_CASE
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2-D K-major tensor map: inner = K elements, rows; box = 128 bytes x box_rows
+static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                      uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * static_cast<uint64_t>(esize)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(128 / esize), box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return n;
+}
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static int max_stages(int na, int N, int kblocks) {
+  const int budget = 227 * 1024 - gemm_extra_smem(N, kblocks);
+  int s = budget / gemm_stage_bytes(na, N);
+  return s > 8 ? 8 : s;
+}
+
+static uint32_t tmem_cols_for(int na, int N) {
+  uint32_t need = static_cast<uint32_t>(2 * na * N), c = 32;
+  while (c < need) c <<= 1;
+  return c;
+}
+
+static int plan_ok(const moe_plan_t* p) {
+  return p && p->abi_version == MOE_ABI_VERSION && p->T >= 0 && p->E >= 1 && p->k >= 1 &&
+         p->tile_n >= 16;
+}
+
+// the common forward; ids_in/w_in non-null selects caller-supplied routing
+static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, const int* ids_in,
+                        const float* w_in, const void* w13, const float* s13, const void* w2,
+                        const float* s2, void* out, void* ws, size_t ws_bytes, void* stream,
+                        void* const* events = nullptr) {
+  if (!plan_ok(p)) return MOE_ERR_INVALID_ARG;
+  const bool fp8 = p->dtype == MOE_DTYPE_FP8_BLOCK128;
+  if (p->T == 0) return MOE_OK;  // empty batch: nothing to read or write
+  if (!x || !w13 || !w2 || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!ids_in && !logits) return MOE_ERR_INVALID_ARG;
+  if (ids_in && !w_in) return MOE_ERR_INVALID_ARG;
+  if (fp8 != (s13 != nullptr) || fp8 != (s2 != nullptr)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) || !aligned16(ws))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < p->workspace_bytes) return MOE_ERR_WORKSPACE;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  auto at = [&](uint64_t off) { return static_cast<void*>(wsb + off); };
+  unsigned* err = static_cast<unsigned*>(at(p->off_err));
+  int* ids = static_cast<int*>(at(p->off_ids));
+  float* topw = static_cast<float*>(at(p->off_w));
+  int* chunk_counts = static_cast<int*>(at(p->off_chunk_counts));
+  int* lrank = static_cast<int*>(at(p->off_lrank));
+  int* counts = static_cast<int*>(at(p->off_counts));
+  int* offsets = static_cast<int*>(at(p->off_offsets));
+  int* chunk_base = static_cast<int*>(at(p->off_chunk_base));
+  int* src = static_cast<int*>(at(p->off_src));
+  int* pos = static_cast<int*>(at(p->off_pos));
+  int4* tiles = static_cast<int4*>(at(p->off_tiles));
+  int* ntiles = static_cast<int*>(at(p->off_ntiles));
+  void* xq = at(p->off_xq);
+  float* xs = static_cast<float*>(at(p->off_xs));
+  void* act = at(p->off_act);
+  float* as = static_cast<float*>(at(p->off_as));
+  float* acc = p->dtype == MOE_DTYPE_F32 ? static_cast<float*>(out)
+                                         : static_cast<float*>(at(p->off_acc));
+
+  const int T = p->T, H = p->H, I = p->I, E = p->E, k = p->k;
+  const long long R = static_cast<long long>(T) * k;
+  auto mark = [&](int i) {
+    if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st);
+  };
+  if (cudaMemsetAsync(err, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+  mark(0);
+
+  // a-1 routing (+ histogram)
+  const size_t route_smem = static_cast<size_t>(p->route_tpc) * k * sizeof(int);
+  const int mode = ids_in ? 2 : 1;
+  if (p->dtype == MOE_DTYPE_F32)
+    launch_route_t<float>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
+                          static_cast<const float*>(logits), T, E, k, p->scoring, p->renorm,
+                          p->route_tpc, mode, ids_in, w_in, ids, topw, chunk_counts, lrank, err);
+  else
+    launch_route_t<__nv_bfloat16>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
+                                  static_cast<const __nv_bfloat16*>(logits), T, E, k, p->scoring,
+                                  p->renorm, p->route_tpc, mode, ids_in, w_in, ids, topw,
+                                  chunk_counts, lrank, err);
+  mark(1);
+  // a-2 / a-3 scan and tile list
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, E, p->tile_n, p->max_tiles,
+                                  chunk_base, counts, offsets, tiles, ntiles, err);
+  mark(2);
+  // a-2 gather
+  const long long acc_elems = static_cast<long long>(T) * H;
+  const unsigned gblocks = static_cast<unsigned>((R * 32 + 255) / 256);
+  if (p->dtype == MOE_DTYPE_F32)
+    gather_kernel<0><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
+                                              p->route_tpc, src, pos, xq, xs, acc, acc_elems);
+  else if (p->dtype == MOE_DTYPE_BF16)
+    gather_kernel<1><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
+                                              p->route_tpc, src, pos, xq, xs, acc, acc_elems);
+  else
+    gather_kernel<2><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
+                                              p->route_tpc, src, pos, xq, xs, acc, acc_elems);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  mark(3);
+
+  // a-4 .. a-7 grouped GEMMs
+  const int kind = p->dtype == MOE_DTYPE_F32 ? KIND_TF32
+                   : p->dtype == MOE_DTYPE_BF16 ? KIND_BF16 : KIND_E4M3;
+  const int esize = kind == KIND_TF32 ? 4 : kind == KIND_BF16 ? 2 : 1;
+  const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  const int N = p->tile_n;
+  CUtensorMap ta1, tb1, ta2, tb2;
+  if (!make_tmap(&ta1, w13, dt, esize, H, static_cast<uint64_t>(E) * 2 * I, 128) ||
+      !make_tmap(&tb1, xq, dt, esize, H, R, N) ||
+      !make_tmap(&ta2, w2, dt, esize, I, static_cast<uint64_t>(E) * H, 128) ||
+      !make_tmap(&tb2, act, dt, esize, I, R, N))
+    return MOE_ERR_CUDA;
+
+  const int sms = sm_count();
+  if (sms <= 0) return MOE_ERR_CUDA;
+  GemmArgs g{};
+  g.tiles = tiles;
+  g.ntiles = ntiles;
+  g.N = N;
+  g.R = static_cast<int>(R);
+  g.I = I;
+  g.H = H;
+  g.k = k;
+  g.src = src;
+  g.topw = topw;
+  g.out_acc = acc;
+  g.err = err;
+  g.limit_ns = kWaitLimitNs;
+
+  // G1: gate+up, SiLU
+  g.mblocks = p->g1_mblocks;
+  g.kblocks = H / (128 / esize);
+  g.a_rows_per_e = 2 * I;
+  g.a_up_off = I;
+  g.m_valid = I;
+  g.stages = max_stages(2, N, g.kblocks);
+  g.tmem_cols = tmem_cols_for(2, N);
+  g.act = act;
+  g.act_scale = as;
+  g.w_scale = s13;
+  g.w_scale_rows_per_e = fp8 ? 2 * I / 128 : 0;
+  g.b_scale = xs;
+  long long work1 = static_cast<long long>(p->max_tiles) * g.mblocks;
+  int grid1 = static_cast<int>(work1 < sms ? work1 : sms);
+  int smem1 = g.stages * gemm_stage_bytes(2, N) + gemm_extra_smem(N, g.kblocks);
+  if (launch_grouped_gemm(kind, 1, g, ta1, tb1, grid1, smem1, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  mark(4);
+
+  // G2: down, weighted combine
+  g.mblocks = p->g2_mblocks;
+  g.kblocks = I / (128 / esize);
+  g.a_rows_per_e = H;
+  g.a_up_off = 0;
+  g.m_valid = H;
+  g.stages = max_stages(1, N, g.kblocks);
+  g.tmem_cols = tmem_cols_for(1, N);
+  g.w_scale = s2;
+  g.w_scale_rows_per_e = fp8 ? H / 128 : 0;
+  g.b_scale = as;
+  long long work2 = static_cast<long long>(p->max_tiles) * g.mblocks;
+  int grid2 = static_cast<int>(work2 < sms ? work2 : sms);
+  int smem2 = g.stages * gemm_stage_bytes(1, N) + gemm_extra_smem(N, g.kblocks);
+  if (launch_grouped_gemm(kind, 2, g, ta2, tb2, grid2, smem2, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  mark(5);
+
+  if (p->dtype != MOE_DTYPE_F32) {
+    const long long n = acc_elems;
+    long long blocks = (n / 4 + 255) / 256;
+    if (blocks > 4L * sms) blocks = 4L * sms;
+    cast_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+        acc, static_cast<__nv_bfloat16*>(out), n);
+  }
+  mark(6);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe
+
+// ====================================================================== C ABI
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_strerror(int code) {
+  switch (code) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape for this dtype";
+    case MOE_ERR_WORKSPACE: return "workspace smaller than plan->workspace_bytes";
+    case MOE_ERR_CUDA: return "CUDA runtime or launch error";
+    case MOE_ERR_DEVICE: return "device error word set (bad or duplicate ids, capacity)";
+    case MOE_ERR_TIMEOUT: return "a device pipeline wait timed out";
+    default: return "unknown error";
+  }
+}
+
+int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm, int force_est,
+             moe_plan_t* plan) {
+  if (!plan) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK ||
+      force_est < 0)
+    return MOE_ERR_INVALID_ARG;
+  if (dtype != MOE_DTYPE_F32 && dtype != MOE_DTYPE_BF16 && dtype != MOE_DTYPE_FP8_BLOCK128)
+    return MOE_ERR_INVALID_ARG;
+  if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+  const int kstep = dtype == MOE_DTYPE_F32 ? 32 : dtype == MOE_DTYPE_BF16 ? 64 : 128;
+  if (H % kstep != 0 || I % kstep != 0) return MOE_ERR_UNSUPPORTED;
+  const long long R = static_cast<long long>(T) * k;
+  if (R > (1ll << 30) || static_cast<long long>(T) * H > (1ll << 40)) return MOE_ERR_INVALID_ARG;
+
+  moe_plan_t p;
+  std::memset(&p, 0, sizeof(p));
+  p.abi_version = MOE_ABI_VERSION;
+  p.T = T;
+  p.H = H;
+  p.I = I;
+  p.E = E;
+  p.k = k;
+  p.dtype = dtype;
+  p.scoring = scoring;
+  p.renorm = renorm ? 1 : 0;
+  p.force_est = force_est;
+  p.route_tpc = T > 2048 ? 32 : 8;
+  p.n_chunks = (T + p.route_tpc - 1) / p.route_tpc;
+  p.g1_mblocks = (I + 127) / 128;
+  p.g2_mblocks = (H + 127) / 128;
+
+  // 1) worst-case capacity, from (T, k, E, H, I, dtype) alone: the tile list
+  //    is bounded with the smallest token tile (16), whatever est says
+  const long long max_tiles = (R + 15) / 16 + (E < R ? E : R) + 1;
+  p.max_tiles = static_cast<int32_t>(max_tiles);
+  const int ex = dtype == MOE_DTYPE_F32 ? 4 : dtype == MOE_DTYPE_BF16 ? 2 : 1;
+  uint64_t off = 0;
+  auto take = [&](uint64_t bytes) {
+    const uint64_t o = off;
+    off += (bytes + 255) & ~static_cast<uint64_t>(255);
+    return o;
+  };
+  p.off_err = take(16);
+  p.off_ids = take(R * 4);
+  p.off_w = take(R * 4);
+  p.off_chunk_counts = take(static_cast<uint64_t>(p.n_chunks) * E * 4);
+  p.off_lrank = take(R * 4);
+  p.off_counts = take(static_cast<uint64_t>(E) * 4);
+  p.off_offsets = take(static_cast<uint64_t>(E + 1) * 4);
+  p.off_chunk_base = take(static_cast<uint64_t>(p.n_chunks) * E * 4);
+  p.off_src = take(R * 4);
+  p.off_pos = take(R * 4);
+  p.off_tiles = take(static_cast<uint64_t>(max_tiles) * 16);
+  p.off_ntiles = take(16);
+  p.off_xq = take(static_cast<uint64_t>(R) * H * ex);
+  p.off_xs = take(dtype == MOE_DTYPE_FP8_BLOCK128 ? static_cast<uint64_t>(R) * (H / 128) * 4 : 0);
+  p.off_act = take(static_cast<uint64_t>(R) * I * ex);
+  p.off_as = take(dtype == MOE_DTYPE_FP8_BLOCK128 ? static_cast<uint64_t>(R) * (I / 128) * 4 : 0);
+  p.off_acc = take(dtype == MOE_DTYPE_F32 ? 0 : static_cast<uint64_t>(T) * H * 4);
+  p.workspace_bytes = off;
+
+  // 2) then the estimate (H20 article, para. 3) and the tile it selects
+  const long long est = force_est > 0 ? force_est : (R + E - 1) / E;
+  p.est = static_cast<int32_t>(est < 1 ? 1 : est);
+  p.tile_n = p.est <= 16 ? 16 : p.est <= 32 ? 32 : p.est <= 64 ? 64 : 128;
+  *plan = p;
+  return MOE_OK;
+}
+
+int moe_plan_describe(const moe_plan_t* p, char* buf, size_t n) {
+  if (!plan_ok(p)) return MOE_ERR_INVALID_ARG;
+  static const char* dn[] = {"f32", "bf16", "fp8_block128"};
+  int len = std::snprintf(
+      buf, buf ? n : 0,
+      "moe_plan T=%d H=%d I=%d E=%d k=%d dtype=%s scoring=%s renorm=%d est=%d%s tile_n=%d "
+      "route_tpc=%d chunks=%d max_tiles=%d g1_blocks=%d g2_blocks=%d workspace=%llu B",
+      p->T, p->H, p->I, p->E, p->k, dn[p->dtype], p->scoring ? "sigmoid" : "softmax", p->renorm,
+      p->est, p->force_est ? " (forced)" : "", p->tile_n, p->route_tpc, p->n_chunks,
+      p->max_tiles, p->g1_mblocks, p->g2_mblocks,
+      static_cast<unsigned long long>(p->workspace_bytes));
+  return len;
+}
+
+int moe_forward(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
+                const float* s13, const void* w2, const float* s2, void* out, void* ws,
+                size_t ws_bytes, void* stream) {
+  if (!logits) return MOE_ERR_INVALID_ARG;
+  return forward_impl(plan, x, logits, nullptr, nullptr, w13, s13, w2, s2, out, ws, ws_bytes,
+                      stream);
+}
+
+int moe_forward_timed(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
+                      const float* s13, const void* w2, const float* s2, void* out, void* ws,
+                      size_t ws_bytes, void* stream, void* const* events, int n_events) {
+  if (!logits || !events || n_events != 7) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < 7; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return forward_impl(plan, x, logits, nullptr, nullptr, w13, s13, w2, s2, out, ws, ws_bytes,
+                      stream, events);
+}
+
+int moe_forward_with_ids(const moe_plan_t* plan, const void* x, const int32_t* ids,
+                         const float* topk_w, const void* w13, const float* s13, const void* w2,
+                         const float* s2, void* out, void* ws, size_t ws_bytes, void* stream) {
+  if (!ids || !topk_w) return MOE_ERR_INVALID_ARG;
+  return forward_impl(plan, x, nullptr, ids, topk_w, w13, s13, w2, s2, out, ws, ws_bytes, stream);
+}
+
+int moe_route_topk(const void* logits, int logits_dtype, int T, int E, int k, int scoring,
+                   int renorm, int32_t* ids, float* w, void* stream) {
+  if (!logits || !ids || !w) return MOE_ERR_INVALID_ARG;
+  if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) return MOE_ERR_INVALID_ARG;
+  if (logits_dtype != MOE_LOGITS_F32 && logits_dtype != MOE_LOGITS_BF16) return MOE_ERR_INVALID_ARG;
+  if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int tpc = 8;
+  dim3 grid((T + tpc - 1) / tpc);
+  if (logits_dtype == MOE_LOGITS_F32)
+    launch_route_t<float>(vpt_for(E), grid, 0, st, static_cast<const float*>(logits), T, E, k,
+                          scoring, renorm ? 1 : 0, tpc, 0, nullptr, nullptr, ids, w, nullptr,
+                          nullptr, nullptr);
+  else
+    launch_route_t<__nv_bfloat16>(vpt_for(E), grid, 0, st,
+                                  static_cast<const __nv_bfloat16*>(logits), T, E, k, scoring,
+                                  renorm ? 1 : 0, tpc, 0, nullptr, nullptr, ids, w, nullptr,
+                                  nullptr, nullptr);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_check(const moe_plan_t* plan, void* ws, uint32_t* bits, void* stream) {
+  if (!plan_ok(plan) || !ws) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned word = 0;
+  unsigned* err = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(ws) + plan->off_err);
+  if (cudaMemcpyAsync(&word, err, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word && cudaMemsetAsync(err, 0, sizeof(unsigned), st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (bits) *bits = word;
+  if (word & MOE_DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+  return word ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+}  // extern "C"

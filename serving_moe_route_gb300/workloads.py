@@ -120,22 +120,22 @@ def make_logits(wl: Workload, x: torch.Tensor | None = None) -> torch.Tensor:
     return z.to(out_dtype)
 
 
-def make_inputs(wl: Workload) -> dict:
-    """All inputs of one workload as CPU tensors.
-
-    x [T,H] (fp32 or bf16), logits [T,E], w13 [E,2I,H], w2 [E,H,I]; for the
-    FP8 workloads w13/w2 are float8_e4m3fn codes with fp32 block scales
-    s13 [E,2I/128,H/128] and s2 [E,H/128,I/128].
-    """
-    T, H, I, E = wl.T, wl.H, wl.I, wl.E
+def make_activations(wl: Workload) -> dict:
+    """x [T,H] (fp32 for the fp32 workload, else bf16) and logits [T,E]."""
     gx = _gen(wl.seed, 0)
     if wl.dtype == F32:
-        x = _normal((T, H), 0.02, gx)
+        x = _normal((wl.T, wl.H), 0.02, gx)
     else:
-        x = _normal((T, H), 1.0, gx, torch.bfloat16)
-    logits = make_logits(wl, x)
+        x = _normal((wl.T, wl.H), 1.0, gx, torch.bfloat16)
+    return {"x": x, "logits": make_logits(wl, x)}
+
+
+def make_weights(wl: Workload) -> dict:
+    """w13 [E,2I,H] and w2 [E,H,I]; for the FP8 workloads float8_e4m3fn
+    codes with fp32 block scales s13 [E,2I/128,H/128] and s2 [E,H/128,I/128].
+    Depends only on (H, I, E, dtype, seed), not on T."""
+    H, I, E = wl.H, wl.I, wl.E
     gw = _gen(wl.seed, 2)
-    out = {"x": x, "logits": logits, "s13": None, "s2": None}
     if wl.dtype in (F32, BF16):
         dt = torch.float32 if wl.dtype == F32 else torch.bfloat16
         w13 = torch.empty(E, 2 * I, H, dtype=dt)
@@ -143,24 +143,30 @@ def make_inputs(wl: Workload) -> dict:
         for e in range(E):  # per expert, to bound the fp32 temporaries
             w13[e] = _normal((2 * I, H), 0.02, gw, dt)
             w2[e] = _normal((H, I), 0.02, gw, dt)
-        out["w13"], out["w2"] = w13, w2
-    else:
-        if H % 128 or I % 128:
-            raise ValueError("FP8 block-scaled weights need H and I multiples of 128")
-        # codes from a clipped normal in code space and one positive fp32
-        # scale per [128,128] block, so that code * scale ~ N(0, 0.02)
-        sigma_code = 112.0
-        w13 = torch.empty(E, 2 * I, H, dtype=torch.float8_e4m3fn)
-        w2 = torch.empty(E, H, I, dtype=torch.float8_e4m3fn)
-        for e in range(E):
-            w13[e] = (torch.randn(2 * I, H, generator=gw) * sigma_code).clamp_(-448, 448).to(
-                torch.float8_e4m3fn)
-            w2[e] = (torch.randn(H, I, generator=gw) * sigma_code).clamp_(-448, 448).to(
-                torch.float8_e4m3fn)
-        base = 0.02 / sigma_code
-        s13 = base * (0.75 + 0.5 * torch.rand(E, 2 * I // 128, H // 128, generator=gw))
-        s2 = base * (0.75 + 0.5 * torch.rand(E, H // 128, I // 128, generator=gw))
-        out.update(w13=w13, w2=w2, s13=s13.float().contiguous(), s2=s2.float().contiguous())
+        return {"w13": w13, "w2": w2, "s13": None, "s2": None}
+    if H % 128 or I % 128:
+        raise ValueError("FP8 block-scaled weights need H and I multiples of 128")
+    # codes from a clipped normal in code space and one positive fp32 scale
+    # per [128,128] block, so that code * scale ~ N(0, 0.02)
+    sigma_code = 112.0
+    w13 = torch.empty(E, 2 * I, H, dtype=torch.float8_e4m3fn)
+    w2 = torch.empty(E, H, I, dtype=torch.float8_e4m3fn)
+    for e in range(E):
+        w13[e] = (torch.randn(2 * I, H, generator=gw) * sigma_code).clamp_(-448, 448).to(
+            torch.float8_e4m3fn)
+        w2[e] = (torch.randn(H, I, generator=gw) * sigma_code).clamp_(-448, 448).to(
+            torch.float8_e4m3fn)
+    base = 0.02 / sigma_code
+    s13 = base * (0.75 + 0.5 * torch.rand(E, 2 * I // 128, H // 128, generator=gw))
+    s2 = base * (0.75 + 0.5 * torch.rand(E, H // 128, I // 128, generator=gw))
+    return {"w13": w13, "w2": w2, "s13": s13.float().contiguous(), "s2": s2.float().contiguous()}
+
+
+def make_inputs(wl: Workload) -> dict:
+    """All inputs of one workload as CPU tensors: make_activations and
+    make_weights together."""
+    out = make_activations(wl)
+    out.update(make_weights(wl))
     return out
 
 

@@ -1,0 +1,106 @@
+"""Shared helpers of the GPU parity tests: run a workload through the CUDA
+path (via the C ABI) and through the oracle, compare.  Tolerances:
+bit-exact for ids, counts, offsets, src, pos and tile lists; for outputs
+max|gpu - oracle| <= tol * max|oracle| over the compared tokens, with
+tol = 2e-2 for bf16 and for the TF32 path of the f32 layer, 5e-2 for FP8;
+routing weights within 2e-6 absolute (fp32 exp against the oracle's
+double exp)."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from serving_moe_route_gb300 import MoELayer
+from serving_moe_route_gb300 import workloads as W
+
+TOL = {W.F32: 2e-2, W.BF16: 2e-2, W.FP8: 5e-2}
+W_ATOL = 2e-6
+
+_INPUT_CACHE: dict = {}
+
+
+def inputs(wl: W.Workload) -> dict:
+    key = (wl.T, wl.H, wl.I, wl.E, wl.k, wl.dtype, wl.logits, wl.seed)
+    if key not in _INPUT_CACHE:
+        if len(_INPUT_CACHE) > 2:
+            _INPUT_CACHE.clear()
+        _INPUT_CACHE[key] = W.make_inputs(wl)
+    return _INPUT_CACHE[key]
+
+
+def logits_f32(inp) -> np.ndarray:
+    return inp["logits"].float().numpy()
+
+
+def make_layer(wl, inp) -> MoELayer:
+    dev = torch.device("cuda", 0)
+    s13 = inp["s13"].to(dev) if inp["s13"] is not None else None
+    s2 = inp["s2"].to(dev) if inp["s2"] is not None else None
+    return MoELayer(inp["w13"].to(dev), inp["w2"].to(dev), k=wl.k, dtype=wl.dtype,
+                    scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2, force_est=wl.force_est)
+
+
+def run_gpu(wl, inp, layer=None):
+    layer = layer or make_layer(wl, inp)
+    dev = layer.device
+    x = inp["x"].to(dev)
+    lg = inp["logits"].to(dev)
+    out = layer.forward(x, lg)
+    rc, bits = layer.check(wl.T)
+    assert rc == 0, f"device error word {bits:#x}"
+    inter = {k: v.cpu().numpy().copy() for k, v in layer.intermediates(wl.T).items()}
+    return out.float().cpu().double().numpy(), inter, layer
+
+
+def sample_tokens(wl, inp, n=64, seed=0) -> np.ndarray:
+    if wl.T <= n:
+        return np.arange(wl.T, dtype=np.int32)
+    rng = np.random.default_rng(seed)
+    lg = logits_f32(inp)
+    nan_rows = np.nonzero(np.isnan(lg).all(1))[0][:4]
+    pick = set(range(6)) | set(range(wl.T - 6, wl.T)) | set(nan_rows.tolist())
+    pick |= set(rng.choice(wl.T, n - len(pick), replace=False).tolist())
+    return np.array(sorted(pick)[:n], dtype=np.int32)
+
+
+def run_oracle(wl, inp, tokens):
+    return oracle.moe_forward(
+        T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, dtype=wl.dtype, scoring=wl.scoring,
+        renorm=wl.renorm, x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
+        w13=W.storage_numpy(inp["w13"]), w2=W.storage_numpy(inp["w2"]),
+        s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]), tokens=tokens)
+
+
+def check_routing_and_permutation(wl, inp, inter):
+    """ids / w / counts / offsets / src / pos against the oracle, all tokens."""
+    ids_ref, w_ref = oracle.route(logits_f32(inp), wl.k, scoring=wl.scoring, renorm=wl.renorm)
+    np.testing.assert_array_equal(inter["ids"], ids_ref)
+    np.testing.assert_allclose(inter["w"], w_ref, rtol=0, atol=W_ATOL)
+    counts, offsets, src, pos = oracle.permute(ids_ref.reshape(-1), wl.E)
+    np.testing.assert_array_equal(inter["counts"], counts)
+    np.testing.assert_array_equal(inter["offsets"], offsets)
+    np.testing.assert_array_equal(inter["src"], src)
+    np.testing.assert_array_equal(inter["pos"], pos)
+    # the tile list covers every expert's rows exactly once, in expert order
+    p_tile = None
+    nt = int(inter["ntiles"][0])
+    tiles = inter["tiles"][:nt]
+    rows = np.zeros(wl.E, np.int64)
+    for e, r0, n, _ in tiles:
+        assert 0 <= e < wl.E and 1 <= n
+        assert offsets[e] <= r0 and r0 + n <= offsets[e + 1]
+        rows[e] += n
+        p_tile = n if p_tile is None else max(p_tile, n)
+    np.testing.assert_array_equal(rows, counts)
+    return ids_ref, w_ref
+
+
+def check_outputs(wl, out_gpu, out_ref, tokens):
+    got = out_gpu[tokens]
+    assert np.isfinite(got).all(), "non-finite output"
+    err = np.abs(got - out_ref).max()
+    scale = np.abs(out_ref).max()
+    assert scale > 0
+    assert err <= TOL[wl.dtype] * scale, f"max|err| {err:.3e} > {TOL[wl.dtype]} * {scale:.3e}"
+    return err / scale

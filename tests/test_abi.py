@@ -1,0 +1,121 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every
+symbol the header declares; the header compiles as C and its struct layout
+matches the binding; moe_plan's host arithmetic (estimate, tile table,
+worst-case workspace before the estimate, argument errors).  No compute
+call is made -- there is no GPU here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "moe_route.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from serving_moe_route_gb300 import _binding, _build
+
+    _build.build()
+    _binding.lib()
+    return _binding
+
+
+def _declared():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(moe_\w+)\s*\(", text, re.M)))
+
+
+def test_exports_every_declared_symbol(B):
+    names = _declared()
+    assert set(B.EXPORTED) <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", B.lib_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (moe_\w+)$", out, re.M))
+    for n in names:
+        assert n in exported, n
+        assert hasattr(B.lib(), n)
+
+
+def test_header_is_c_and_layout_matches(B, tmp_path):
+    src = tmp_path / "layout.c"
+    src.write_text(
+        '#include <stdio.h>\n#include <stddef.h>\n#include "moe_route.h"\n'
+        "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(moe_plan_t),"
+        " offsetof(moe_plan_t, workspace_bytes), offsetof(moe_plan_t, off_acc),"
+        " offsetof(moe_plan_t, tile_n)); return 0;}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
+                    str(src), "-o", str(exe)], check=True)
+    vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
+                                           check=True).stdout.split()]
+    P = B.MoePlan
+    assert vals == [ctypes.sizeof(P), P.workspace_bytes.offset, P.off_acc.offset,
+                    P.tile_n.offset]
+
+
+def test_plan_estimate_worked_example(B):
+    # 288 tokens x top-6 over 400 experts: 4.32 rows per expert -> 5
+    p = B.moe_plan(288, 2048, 768, 400, 6, B.MOE_DTYPE_BF16)
+    assert p.est == 5 and p.tile_n == 16
+    old = B.moe_plan(288, 2048, 768, 400, 6, B.MOE_DTYPE_BF16, force_est=288)
+    assert old.est == 288 and old.tile_n == 128
+    # capacity is fixed before the estimate: identical workspace either way
+    assert old.workspace_bytes == p.workspace_bytes
+    assert old.max_tiles == p.max_tiles
+
+
+@pytest.mark.parametrize("T,est,tile", [(1, 1, 16), (2, 1, 16), (4, 1, 16), (16, 1, 16),
+                                        (64, 4, 16), (128, 8, 16), (256, 16, 16),
+                                        (1024, 64, 64), (4096, 256, 128), (512, 32, 32)])
+def test_plan_tile_table(B, T, est, tile):
+    p = B.moe_plan(T, 2048, 768, 128, 8, B.MOE_DTYPE_FP8_BLOCK128)
+    assert p.est == est and p.tile_n == tile
+    assert p.g1_mblocks == 6 and p.g2_mblocks == 16
+    assert p.max_tiles >= -(-T * 8 // 16) + min(128, T * 8)
+
+
+def test_plan_workspace_layout(B):
+    p = B.moe_plan(128, 2048, 768, 128, 8, B.MOE_DTYPE_BF16)
+    offs = [p.off_err, p.off_ids, p.off_w, p.off_chunk_counts, p.off_lrank, p.off_counts,
+            p.off_offsets, p.off_chunk_base, p.off_src, p.off_pos, p.off_tiles, p.off_ntiles,
+            p.off_xq, p.off_xs, p.off_act, p.off_as, p.off_acc]
+    assert all(o % 256 == 0 for o in offs)
+    assert offs == sorted(offs)
+    R = 128 * 8
+    assert p.off_act - p.off_xq >= R * 2048 * 2
+    assert p.workspace_bytes - p.off_acc >= 128 * 2048 * 4
+    assert "est=8" in p.describe() and "tile_n=16" in p.describe()
+
+
+@pytest.mark.parametrize("args,code", [
+    ((16, 128, 64, 8, 0, 1), -1),      # k = 0
+    ((16, 128, 64, 8, 9, 1), -1),      # k > E
+    ((16, 128, 64, 2000, 8, 1), -1),   # E > 1024
+    ((-1, 128, 64, 8, 2, 1), -1),      # T < 0
+    ((16, 128, 64, 8, 2, 7), -1),      # bad dtype
+    ((16, 96, 64, 8, 2, 1), -2),       # H not a multiple of 64 for bf16
+    ((16, 128, 64, 8, 2, 2), -2),      # I not a multiple of 128 for fp8
+    ((16, 100, 64, 8, 2, 0), -2),      # H not a multiple of 32 for f32
+])
+def test_plan_rejects(B, args, code):
+    p = B.MoePlan()
+    rc = B.lib().moe_plan(*args, 0, 1, 0, ctypes.byref(p))
+    assert rc == code
+    assert B.strerror(rc)
+
+
+def test_forward_validates_before_launch(B):
+    p = B.moe_plan(16, 128, 64, 8, 2, B.MOE_DTYPE_BF16)
+    # null pointers and short workspace are rejected on the host: no launch
+    assert B.moe_forward(p, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0) == B.MOE_ERR_INVALID_ARG
+    fake = 1 << 20  # never dereferenced: validation fails first
+    assert B.moe_forward(p, fake, fake, fake, 0, fake, 0, fake, fake, 16, 0) == \
+        B.MOE_ERR_WORKSPACE
+    assert B.moe_forward(p, fake + 4, fake, fake, 0, fake, 0, fake, fake,
+                         p.workspace_bytes, 0) == B.MOE_ERR_INVALID_ARG
+    assert B.moe_forward(p, fake, fake, fake, fake, fake, 0, fake, fake, p.workspace_bytes,
+                         0) == B.MOE_ERR_INVALID_ARG  # scales given to a bf16 layer
+    assert B.moe_route_topk(fake, 1, 4, 8, 9, 0, 1, fake, fake, 0) == B.MOE_ERR_INVALID_ARG

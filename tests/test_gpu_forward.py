@@ -1,0 +1,153 @@
+"""GPU parity of the whole layer (moe_forward through the C ABI) against the
+oracle on the workloads of the pages and on edge cases: routing and
+permutation bit-exact on every token, outputs within tolerance on all
+tokens (small cases) or on a sampled set of tokens (full-size cases)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity_util as PU
+from serving_moe_route_gb300 import MoELayer
+from serving_moe_route_gb300 import workloads as W
+from serving_moe_route_gb300 import _binding as B
+
+pytestmark = pytest.mark.gpu
+
+WL = W.workloads()
+
+FULL = ["tiny_f32", "decode_bf16", "sparse_uniform_bf16", "sparse_concentrated_bf16",
+        "sparse_uniform_bf16_old_est", "fp8_T1", "fp8_T2", "fp8_T16", "fp8_T64", "fp8_T128",
+        "fp8_T1024", "fp8_T4096", "skewed_prefill_bf16", "skewed_prefill_sigmoid_bf16"]
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_forward_workload(name):
+    wl = WL[name]
+    inp = PU.inputs(wl)
+    out, inter, _ = PU.run_gpu(wl, inp)
+    PU.check_routing_and_permutation(wl, inp, inter)
+    tokens = PU.sample_tokens(wl, inp, n=48 if wl.T > 1024 else 64)
+    ref, ids_o, _ = PU.run_oracle(wl, inp, tokens)
+    np.testing.assert_array_equal(inter["ids"][tokens], ids_o)
+    PU.check_outputs(wl, out, ref, tokens)
+
+
+EDGE = [
+    # ragged: E not a multiple of 32, T not a multiple of the routing chunk
+    W.custom("ragged_bf16", T=37, H=256, I=128, E=40, k=3, dtype=W.BF16, seed=21),
+    W.custom("ragged_fp8", T=37, H=256, I=128, E=40, k=3, dtype=W.FP8, seed=22),
+    W.custom("ragged_f32", T=29, H=96, I=64, E=12, k=4, dtype=W.F32, seed=23),
+    W.custom("single_token", T=1, H=2048, I=768, E=128, k=8, dtype=W.BF16, seed=24),
+    W.custom("k1", T=50, H=128, I=128, E=16, k=1, dtype=W.BF16, seed=25),
+    W.custom("one_expert", T=33, H=128, I=64, E=1, k=1, dtype=W.BF16, seed=26),
+    W.custom("all_nan", T=40, H=256, I=128, E=64, k=8, dtype=W.BF16, seed=27, logits="nan_rows"),
+    W.custom("sigmoid_no_renorm", T=45, H=256, I=128, E=64, k=4, dtype=W.BF16, seed=28,
+             scoring=W.SIGMOID, renorm=False),
+    W.custom("softmax_no_renorm", T=45, H=256, I=128, E=64, k=4, dtype=W.FP8, seed=29,
+             renorm=False),
+    W.custom("many_tiles", T=600, H=256, I=256, E=8, k=2, dtype=W.BF16, seed=30),
+    W.custom("big_tiles_fp8", T=300, H=256, I=256, E=4, k=2, dtype=W.FP8, seed=31),
+    W.custom("forced_est", T=100, H=256, I=128, E=64, k=4, dtype=W.BF16, seed=32, force_est=100),
+    W.custom("prefill_chunks", T=2500, H=128, I=128, E=32, k=4, dtype=W.BF16, seed=33),
+]
+
+
+@pytest.mark.parametrize("wl", EDGE, ids=[w.name for w in EDGE])
+def test_forward_edge(wl):
+    inp = W.make_inputs(wl)
+    if wl.name == "all_nan":
+        inp["logits"][:] = float("nan")
+    out, inter, _ = PU.run_gpu(wl, inp)
+    PU.check_routing_and_permutation(wl, inp, inter)
+    tokens = PU.sample_tokens(wl, inp, n=128)
+    ref, _, _ = PU.run_oracle(wl, inp, tokens)
+    PU.check_outputs(wl, out, ref, tokens)
+
+
+def test_all_tokens_on_the_same_experts():
+    # every token routed to the same k experts: the crash repro shape of
+    # PR #39593 (one expert gets T rows, the rest none)
+    wl = W.custom("same_experts", T=300, H=256, I=128, E=64, k=4, dtype=W.BF16, seed=34)
+    inp = W.make_inputs(wl)
+    lg = torch.zeros(wl.T, wl.E)
+    lg[:, [5, 17, 2, 60]] = torch.tensor([4.0, 3.0, 2.0, 1.0])
+    inp["logits"] = lg.to(torch.bfloat16)
+    out, inter, _ = PU.run_gpu(wl, inp)
+    PU.check_routing_and_permutation(wl, inp, inter)
+    assert sorted(np.nonzero(inter["counts"])[0].tolist()) == [2, 5, 17, 60]
+    tokens = PU.sample_tokens(wl, inp, n=64)
+    ref, _, _ = PU.run_oracle(wl, inp, tokens)
+    PU.check_outputs(wl, out, ref, tokens)
+
+
+def test_fp8_activation_quantisation_bit_exact():
+    wl = WL["fp8_T16"]
+    inp = PU.inputs(wl)
+    _, inter, _ = PU.run_gpu(wl, inp)
+    x = inp["x"].float().numpy()
+    src = inter["src"]
+    for slot in range(wl.T * wl.k):
+        t = src[slot] // wl.k
+        codes, scales = oracle.quant_group128(x[t])
+        np.testing.assert_array_equal(inter["xq"][slot], codes)
+        np.testing.assert_array_equal(inter["xs"][slot], scales)
+
+
+def test_empty_batch_enqueues_nothing():
+    wl = W.custom("empty", T=0, H=256, I=128, E=8, k=2, dtype=W.BF16, seed=35)
+    dev = torch.device("cuda", 0)
+    inp = W.make_inputs(W.custom(T=1, H=256, I=128, E=8, k=2, dtype=W.BF16, seed=35))
+    layer = PU.make_layer(wl, inp)
+    out = layer.forward(torch.empty(0, 256, dtype=torch.bfloat16, device=dev),
+                        torch.empty(0, 8, dtype=torch.bfloat16, device=dev))
+    assert out.shape == (0, 256)
+
+
+def test_repeated_calls_are_stable_and_layer_reuses_workspace():
+    wl = W.custom("repeat", T=64, H=256, I=128, E=16, k=4, dtype=W.BF16, seed=36)
+    inp = W.make_inputs(wl)
+    layer = PU.make_layer(wl, inp)
+    a, _, _ = PU.run_gpu(wl, inp, layer)
+    b, _, _ = PU.run_gpu(wl, inp, layer)
+    # only the order of the fp32 combine additions may differ between calls
+    np.testing.assert_allclose(a, b, rtol=0, atol=1e-2 * np.abs(a).max())
+
+
+def test_with_ids_matches_routed_forward():
+    wl = W.custom("with_ids", T=64, H=256, I=128, E=32, k=4, dtype=W.BF16, seed=37)
+    inp = W.make_inputs(wl)
+    out, inter, layer = PU.run_gpu(wl, inp)
+    dev = layer.device
+    ids = torch.from_numpy(inter["ids"]).to(dev)
+    w = torch.from_numpy(inter["w"]).to(dev)
+    out2 = layer.forward_with_ids(inp["x"].to(dev), ids, w)
+    rc, bits = layer.check(wl.T)
+    assert rc == 0 and bits == 0
+    o2 = out2.float().cpu().double().numpy()
+    np.testing.assert_allclose(o2, out, rtol=0, atol=1e-2 * np.abs(out).max())
+
+
+def test_with_ids_reports_bad_and_duplicate_ids():
+    # duplicate / out-of-range ids are reported in the error word and skipped,
+    # never used as an index (the PR #39593 failure mode)
+    wl = W.custom("bad_ids", T=32, H=256, I=128, E=16, k=4, dtype=W.BF16, seed=38)
+    inp = W.make_inputs(wl)
+    layer = PU.make_layer(wl, inp)
+    dev = layer.device
+    ids = torch.tensor([[0, 1, 2, 3]] * wl.T, dtype=torch.int32)
+    ids[3] = torch.tensor([7, 7, 7, 7])          # duplicates
+    ids[9] = torch.tensor([1, 99, -4, 2])        # out of range
+    w = torch.full((wl.T, wl.k), 0.25)
+    out = layer.forward_with_ids(inp["x"].to(dev), ids.to(dev), w.to(dev))
+    rc, bits = layer.check(wl.T)
+    assert rc == B.MOE_ERR_DEVICE
+    assert bits & B.MOE_DEVERR_DUP_ID and bits & B.MOE_DEVERR_BAD_ID
+    inter = layer.intermediates(wl.T)
+    got_ids = inter["ids"].cpu().numpy()
+    assert list(got_ids[3]) == [7, -1, -1, -1]
+    assert list(got_ids[9]) == [1, -1, -1, 2]
+    assert int(inter["counts"].sum()) == wl.T * wl.k - 5
+    assert torch.isfinite(out.float()).all()
+    # the context is still healthy: a normal call succeeds afterwards
+    PU.run_gpu(wl, inp, layer)
