@@ -176,7 +176,13 @@ class Runner:
         self.out_h = torch.empty(wl.T, wl.H, dtype=self.x.dtype).pin_memory()
 
     def _events(self, n):
-        return [[self.torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
+        # torch creates the CUDA event lazily: record each once so that its
+        # handle exists before the library records it again
+        evs = [[self.torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
+        for row in evs:
+            for e in row:
+                e.record(self.stream)
+        return evs
 
     def step_timed(self, ev):
         from serving_moe_route_gb300 import _binding as B

@@ -96,8 +96,10 @@ extern "C" {
  *   tiles   int32 [max_tiles, 4]  {expert, first row, rows, 0} token tiles
  *   ntiles  int32 [1]       number of valid tiles
  *   err     uint32 [1]      device error word (MOE_DEVERR_* bits)
- * The remaining regions (chunk counts, permuted activations, scales, the
- * fp32 combine accumulator) are internal.
+ *   y       [T*k, H]        routing-weighted expert output per permuted
+ *                           row (bf16; f32 for the f32 layer)
+ * The remaining regions (chunk counts, permuted activations, scales) are
+ * internal.
  */
 typedef struct moe_plan {
   int32_t abi_version;
@@ -105,7 +107,9 @@ typedef struct moe_plan {
   int32_t dtype, scoring, renorm;
   int32_t est;        /* rows-per-expert estimate used for the tile choice */
   int32_t force_est;  /* 0, or the caller's override (e.g. T: old estimate) */
-  int32_t tile_n;     /* token tile = MMA N (16, 32, 64 or 128) */
+  int32_t tile_n;     /* token tile = MMA N (16, 32, 64 or 128) from est; the
+                         device widens it per expert for BF16/F32 (an expert
+                         with more rows gets 32 / 64 / 128) */
   int32_t route_tpc;  /* tokens per routing CTA */
   int32_t n_chunks;   /* routing CTAs = ceil(T / route_tpc) */
   int32_t max_tiles;  /* worst-case token tiles (independent of est) */
@@ -115,7 +119,7 @@ typedef struct moe_plan {
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;
-  uint64_t off_xq, off_xs, off_act, off_as, off_acc;
+  uint64_t off_xq, off_xs, off_act, off_as, off_y;
   uint64_t reserved1[4];
 } moe_plan_t;
 

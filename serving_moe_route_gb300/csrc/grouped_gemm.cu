@@ -3,10 +3,11 @@
 //
 // One persistent CTA per SM walks a device-built list of work items
 // (token tile x 128-row weight block).  Swap-AB orientation: the MMA's M
-// side is 128 rows of one expert's weight matrix, its N side a tile of
-// `N` permuted token rows of that expert (N = 16 .. 128 chosen from the
-// rows-per-expert estimate, H20 article para. 3), so a decode-sized expert
-// with a handful of rows still fills the 128-wide M side with weights.
+// side is 128 rows of one expert's weight matrix, its N side a tile of n
+// permuted token rows of that expert, n = 16 .. 128 set per expert from its
+// row count with the rows-per-expert estimate as the floor (H20 article,
+// para. 3), so a decode-sized expert with a handful of rows still fills the
+// 128-wide M side with weights and a hot expert gets wide tiles.
 //
 //   warp 0      TMA producer: weight tile(s) + token tile per 128-byte K step
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
@@ -14,12 +15,13 @@
 //                 G1: act = SiLU(gate) * up  (FP8: + per-token 128-group
 //                     e4m3 quantisation, clamp with fminf/fmaxf as in
 //                     PR #39593 "Purpose")
-//                 G2: out_acc[t] += w[t,j] * y  (the top-k weighted combine)
+//                 G2: ybuf[row] = w[t,j] * y  (the combine's weighting; the
+//                     k rows of a token are summed by the combine kernel)
 //
 // FP8 [128,128] block scales (Lab notes #6, config file line): each 128-K
-// block is accumulated into its own TMEM buffer (double-buffered) and the
-// epilogue warps fold it into fp32 registers with weight-scale x
-// activation-scale, so arbitrary fp32 scales are honoured exactly.
+// block is accumulated into its own TMEM slot (up to 16 slots in flight) and
+// the epilogue warps fold it into fp32 registers with the product
+// weight-scale x activation-scale, so arbitrary fp32 scales are honoured.
 //
 // Every wait is bounded (see mbar_wait); a timeout sets MOE_DEVERR_TIMEOUT
 // in the error word, raises a CTA-wide abort flag, drains in-flight copies
@@ -34,7 +36,8 @@ namespace moe {
 
 constexpr int kThreads = 320;
 constexpr int kEpiThreads = 256;
-constexpr int kMaxHalf = 64;  // columns per epilogue thread at tile_n = 128
+constexpr int kMaxHalf = 64;  // columns per epilogue thread at n = 128
+constexpr int kMaxSlots = 16;
 constexpr unsigned kDevErrTimeout = 4u;
 
 template <int KIND>
@@ -57,15 +60,13 @@ struct KindTraits<KIND_E4M3> {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
+// activation (G1 output) and weighted expert output (G2 output) stores
 template <int KIND>
-__device__ __forceinline__ void store_act(void* act, size_t idx, float v);
-template <>
-__device__ __forceinline__ void store_act<KIND_TF32>(void* act, size_t idx, float v) {
-  static_cast<float*>(act)[idx] = v;
-}
-template <>
-__device__ __forceinline__ void store_act<KIND_BF16>(void* act, size_t idx, float v) {
-  static_cast<__nv_bfloat16*>(act)[idx] = __float2bfloat16_rn(v);
+__device__ __forceinline__ void store_val(void* base, size_t idx, float v) {
+  if constexpr (KIND == KIND_TF32)
+    static_cast<float*>(base)[idx] = v;
+  else
+    static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
 }
 
 template <int KIND, int G>
@@ -79,9 +80,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int N = args.N;
   const int S = args.stages;
-  const uint32_t stage_bytes = NA * 16384u + static_cast<uint32_t>(N) * 128u;
+  const int NS = args.nslots;
+  const int NM = args.n_max;
+  const uint32_t stage_bytes = NA * 16384u + static_cast<uint32_t>(NM) * 128u;
+  const uint32_t slot_cols = static_cast<uint32_t>(NA * NM);
   const uint64_t limit = args.limit_ns;
 
   // ---- shared memory carve-up (stage ring 1024-aligned for 128B swizzle)
@@ -89,21 +92,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + static_cast<size_t>(S) * stage_bytes);
   uint64_t* empty = full + S;
-  uint64_t* accf = empty + S;  // [2] accumulator (or FP8 partial) ready
-  uint64_t* acce = accf + 2;   // [2] accumulator drained by the epilogue
-  uint64_t* done = acce + 2;   // all MMAs of this CTA complete
-  uint64_t* epib = done + 1;   // epilogue-internal barrier
+  uint64_t* accf = empty + S;     // [NS] accumulator slot written by the MMAs
+  uint64_t* acce = accf + NS;     // [NS] accumulator slot drained by the epilogue
+  uint64_t* done = acce + NS;     // all MMAs of this CTA complete
+  uint64_t* epib = done + 1;      // epilogue-internal barrier
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epib + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* sb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 256);  // [N][kblocks]
-  float* red = sb + N * args.kblocks;                                             // [4][N]
+  float* cs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [NA][kb][NM]
+  float* red = cs + NA * args.kblocks * NM;                                      // [4][NM]
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < NS; ++b) {
       mbar_init(smem_u32(&accf[b]), 1);
       mbar_init(smem_u32(&acce[b]), kEpiThreads);
     }
@@ -138,7 +141,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
         const int4 tile = args.tiles[w / args.mblocks];
         const int mb = w % args.mblocks;
+        const int n = tile.w;
         const int a_row = tile.x * args.a_rows_per_e + mb * 128;
+        const uint32_t tx = NA * 16384u + static_cast<uint32_t>(n) * 128u;
         for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1u) ^ 1u, limit, abort_flag)) {
@@ -147,11 +152,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           uint8_t* st = stages + static_cast<size_t>(s) * stage_bytes;
           const uint32_t fb = smem_u32(&full[s]);
-          mbar_arrive_expect_tx(fb, stage_bytes);
+          mbar_arrive_expect_tx(fb, tx);
           const int kx = kb * BKE;
           tma_load_2d(smem_u32(st), &tma_a, fb, kx, a_row, pol_w);
           if (NA == 2) tma_load_2d(smem_u32(st + 16384), &tma_a, fb, kx, a_row + args.a_up_off, pol_w);
-          tma_load_2d(smem_u32(st + NA * 16384), &tma_b, fb, kx, tile.y, pol_x);
+          for (int b = 0; b < n; b += kTokBox)
+            tma_load_2d(smem_u32(st + NA * 16384 + b * 128), &tma_b, fb, kx, tile.y + b, pol_x);
         }
       }
       if (!ok) {
@@ -166,18 +172,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(N));
       uint32_t it = 0, tc = 0, kc = 0;
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+        const int n = args.tiles[w / args.mblocks].w;
+        const uint32_t idesc = idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(n));
         uint32_t dbase = 0;
         if (!FP8) {
-          const uint32_t buf = tc & 1u;
-          if (!mbar_wait(smem_u32(&acce[buf]), ((tc >> 1) & 1u) ^ 1u, limit, abort_flag)) {
+          const uint32_t sl = tc % NS;
+          if (!mbar_wait(smem_u32(&acce[sl]), ((tc / NS) & 1u) ^ 1u, limit, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          dbase = buf * NA * N;
+          dbase = sl * slot_cols;
         }
         for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
@@ -186,15 +193,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          uint32_t pb = 0;
+          uint32_t sl = 0;
           if (FP8) {
-            pb = kc & 1u;
-            if (!mbar_wait(smem_u32(&acce[pb]), ((kc >> 1) & 1u) ^ 1u, limit, abort_flag)) {
+            sl = kc % NS;
+            if (!mbar_wait(smem_u32(&acce[sl]), ((kc / NS) & 1u) ^ 1u, limit, abort_flag)) {
               ok = false;
               break;
             }
             tc_fence_after();
-            dbase = pb * NA * N;
+            dbase = sl * slot_cols;
           }
           const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * stage_bytes);
 #pragma unroll
@@ -204,18 +211,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint64_t ad = sdesc_sw128(sa + a * 16384 + ks * 32);
               const uint64_t bd = sdesc_sw128(sa + NA * 16384 + ks * 32);
               const uint32_t accumulate = FP8 ? (ks != 0) : ((kb | ks) != 0);
-              mma_issue<KIND>(tmem_base + dbase + a * N, ad, bd, idesc, accumulate);
+              mma_issue<KIND>(tmem_base + dbase + a * NM, ad, bd, idesc, accumulate);
             }
           }
           mma_commit(smem_u32(&empty[s]));  // frees the stage once read
           if (FP8) {
-            mma_commit(smem_u32(&accf[pb]));
+            mma_commit(smem_u32(&accf[sl]));
             ++kc;
           }
         }
         if (!ok) break;
         if (!FP8) {
-          mma_commit(smem_u32(&accf[tc & 1u]));
+          mma_commit(smem_u32(&accf[tc % NS]));
           ++tc;
         }
       }
@@ -233,8 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2;
     const int q = warp & 3;     // TMEM lane quadrant this warp may read
     const int half = ew >> 2;   // which half of the token columns
-    const int hc = N >> 1;      // columns per thread
-    const int c_begin = half * hc;
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t tc = 0, kc = 0, eb = 0;
@@ -249,32 +254,34 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
       const int4 tile = args.tiles[w / args.mblocks];
       const int mb = w % args.mblocks;
-      const int row0 = tile.y, nrows = tile.z;
+      const int row0 = tile.y, nrows = tile.z, n = tile.w;
+      const int hc = n >> 1;  // columns per thread
+      const int c_begin = half * hc;
       const int row = mb * 128 + r_in_tile;  // weight row = output feature
       const bool row_ok = row < args.m_valid;
 
       if constexpr (!FP8) {
-        const uint32_t buf = tc & 1u;
-        const bool got = mbar_wait(smem_u32(&accf[buf]), (tc >> 1) & 1u, limit, abort_flag);
+        const uint32_t sl = tc % NS;
+        const bool got = mbar_wait(smem_u32(&accf[sl]), (tc / NS) & 1u, limit, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const uint32_t dcol = buf * NA * N;
+        const uint32_t dcol = sl * slot_cols;
         for (int c0 = 0; c0 < hc; c0 += 8) {
           const int cc = c_begin + c0;
           if constexpr (G == 1) {
             float gv[8], uv[8];
             tmem_ld8(lane_addr + dcol + cc, gv);
-            tmem_ld8(lane_addr + dcol + N + cc, uv);
+            tmem_ld8(lane_addr + dcol + NM + cc, uv);
             tmem_wait_ld(gv, uv);
             if (row_ok) {
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) {
                 const int j = cc + jj;
                 if (j < nrows)
-                  store_act<KIND>(args.act, static_cast<size_t>(row0 + j) * args.I + row,
+                  store_val<KIND>(args.act, static_cast<size_t>(row0 + j) * args.I + row,
                                   silu_f(gv[jj]) * uv[jj]);
               }
             }
@@ -287,28 +294,32 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int jj = 0; jj < 8; ++jj) {
                 const int j = cc + jj;
                 if (j < nrows) {
-                  const int f = __ldg(args.src + row0 + j);
-                  const int t = f / args.k;
-                  atomicAdd(args.out_acc + static_cast<size_t>(t) * args.H + row,
-                            __ldg(args.topw + f) * yv[jj]);
+                  const float wt = __ldg(args.topw + __ldg(args.src + row0 + j));
+                  store_val<KIND>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
+                                  wt * yv[jj]);
                 }
               }
             }
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&acce[buf]));
+        mbar_arrive(smem_u32(&acce[sl]));
         ++tc;
       } else {
-        // -------- FP8: stage this tile's activation scales [N][kblocks]
+        // -------- FP8: per-column scale products cs[a][kb][j] = s_w[a][kb] * s_x[j][kb]
         const int kbs = args.kblocks;
         if (!ep_barrier()) {
           ok = false;
           break;
         }
-        for (int i = ew * 32 + lane; i < N * kbs; i += kEpiThreads) {
-          const int j = i / kbs;
-          sb[i] = (j < nrows) ? __ldg(args.b_scale + static_cast<size_t>(row0 + j) * kbs + (i % kbs))
+        const float* sw = args.w_scale +
+                          (static_cast<size_t>(tile.x) * args.w_scale_rows_per_e + mb) * kbs;
+        for (int i = ew * 32 + lane; i < NA * kbs * NM; i += kEpiThreads) {
+          const int a = i / (kbs * NM);
+          const int kb = (i / NM) % kbs;
+          const int j = i % NM;
+          const float swv = __ldg(sw + static_cast<size_t>(a) * (args.I / 128) * kbs + kb);
+          cs[i] = (j < nrows) ? swv * __ldg(args.b_scale + static_cast<size_t>(row0 + j) * kbs + kb)
                               : 0.0f;
         }
         if (!ep_barrier()) {
@@ -321,20 +332,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc0[c] = 0.0f;
           acc1[c] = 0.0f;
         }
-        const float* sw0 =
-            args.w_scale + (static_cast<size_t>(tile.x) * args.w_scale_rows_per_e + mb) * kbs;
-        const float* sw1 = sw0 + static_cast<size_t>(args.I / 128) * kbs;  // up rows (G1)
         for (int kb = 0; kb < kbs; ++kb, ++kc) {
-          const uint32_t pb = kc & 1u;
-          const bool got = mbar_wait(smem_u32(&accf[pb]), (kc >> 1) & 1u, limit, abort_flag);
+          const uint32_t sl = kc % NS;
+          const bool got = mbar_wait(smem_u32(&accf[sl]), (kc / NS) & 1u, limit, abort_flag);
           if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const float s0 = __ldg(sw0 + kb);
-          const float s1 = (NA == 2) ? __ldg(sw1 + kb) : 0.0f;
-          const uint32_t dcol = pb * NA * N;
+          const uint32_t dcol = sl * slot_cols;
+          const float* c0p = cs + kb * NM;
+          const float* c1p = cs + (kbs + kb) * NM;
 #pragma unroll
           for (int c0 = 0; c0 < kMaxHalf; c0 += 8) {
             if (c0 < hc) {
@@ -342,21 +350,27 @@ __global__ void __launch_bounds__(kThreads, 1)
               float p0[8], p1[8];
               tmem_ld8(lane_addr + dcol + cc, p0);
               if (NA == 2) {
-                tmem_ld8(lane_addr + dcol + N + cc, p1);
+                tmem_ld8(lane_addr + dcol + NM + cc, p1);
                 tmem_wait_ld(p0, p1);
               } else {
                 tmem_wait_ld(p0);
               }
+              const float4 s0a = *reinterpret_cast<const float4*>(c0p + cc);
+              const float4 s0b = *reinterpret_cast<const float4*>(c0p + cc + 4);
+              const float s0[8] = {s0a.x, s0a.y, s0a.z, s0a.w, s0b.x, s0b.y, s0b.z, s0b.w};
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                const float bs = sb[(cc + jj) * kbs + kb];
-                acc0[c0 + jj] = fmaf(p0[jj], s0 * bs, acc0[c0 + jj]);
-                if (NA == 2) acc1[c0 + jj] = fmaf(p1[jj], s1 * bs, acc1[c0 + jj]);
+              for (int jj = 0; jj < 8; ++jj) acc0[c0 + jj] = fmaf(p0[jj], s0[jj], acc0[c0 + jj]);
+              if (NA == 2) {
+                const float4 s1a = *reinterpret_cast<const float4*>(c1p + cc);
+                const float4 s1b = *reinterpret_cast<const float4*>(c1p + cc + 4);
+                const float s1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
+#pragma unroll
+                for (int jj = 0; jj < 8; ++jj) acc1[c0 + jj] = fmaf(p1[jj], s1[jj], acc1[c0 + jj]);
               }
             }
           }
           tc_fence_before();
-          mbar_arrive(smem_u32(&acce[pb]));
+          mbar_arrive(smem_u32(&acce[sl]));
         }
         if (!ok) break;
 
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int off = 16; off > 0; off >>= 1)
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-              if (lane == 0) red[q * N + c_begin + c] = m;
+              if (lane == 0) red[q * NM + c_begin + c] = m;
             }
           }
           if (!ep_barrier()) {
@@ -385,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int j = c_begin + c;
               if (j < nrows) {
                 const float amax =
-                    fmaxf(fmaxf(red[j], red[N + j]), fmaxf(red[2 * N + j], red[3 * N + j]));
+                    fmaxf(fmaxf(red[j], red[NM + j]), fmaxf(red[2 * NM + j], red[3 * NM + j]));
                 const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
                 float v = __fdiv_rn(acc0[c], scale);
                 v = fmaxf(fminf(v, 448.0f), -448.0f);
@@ -402,10 +416,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (c < hc) {
               const int j = c_begin + c;
               if (j < nrows && row_ok) {
-                const int f = __ldg(args.src + row0 + j);
-                const int t = f / args.k;
-                atomicAdd(args.out_acc + static_cast<size_t>(t) * args.H + row,
-                          __ldg(args.topw + f) * acc0[c]);
+                const float wt = __ldg(args.topw + __ldg(args.src + row0 + j));
+                store_val<KIND_BF16>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
+                                     wt * acc0[c]);
               }
             }
           }
@@ -440,6 +453,7 @@ static cudaError_t launch_one(const GemmArgs& args, const CUtensorMap& ta, const
 
 cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const CUtensorMap& ta,
                                 const CUtensorMap& tb, int grid, int smem, cudaStream_t stream) {
+  if (args.nslots < 1 || args.nslots > kMaxSlots) return cudaErrorInvalidValue;
   if (kind == KIND_TF32) {
     return g == 1 ? launch_one<KIND_TF32, 1>(args, ta, tb, grid, smem, stream)
                   : launch_one<KIND_TF32, 2>(args, ta, tb, grid, smem, stream);

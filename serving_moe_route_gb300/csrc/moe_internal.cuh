@@ -10,30 +10,34 @@ namespace moe {
 // operand element kinds of the grouped GEMMs
 enum GemmKind : int { KIND_TF32 = 0, KIND_BF16 = 1, KIND_E4M3 = 2 };
 
+// TMA box height of the token-tile loads: a tile of n rows is n/16 boxes
+constexpr int kTokBox = 16;
+
 // Arguments of one grouped GEMM launch (swap-AB orientation: the MMA's M
-// side is 128 weight rows of one expert, its N side is a tile of up to
-// tile_n permuted token rows of that expert).
+// side is 128 weight rows of one expert, its N side a tile of up to
+// n_max permuted token rows of that expert; each tile carries its own n).
 struct GemmArgs {
-  const int4* tiles;   // [max_tiles] {expert, first permuted row, rows, 0}
+  const int4* tiles;   // [max_tiles] {expert, first permuted row, rows, tile n}
   const int* ntiles;   // device count of valid tiles
   int mblocks;         // 128-row weight blocks per expert (G1: ceil(I/128))
   int kblocks;         // K / (128 bytes / element size)
-  int N;               // token tile = MMA N
+  int n_max;           // largest tile n (stage and TMEM slot size)
   int a_rows_per_e;    // rows of one expert in the A view (G1: 2I, G2: H)
   int a_up_off;        // G1: I (first up row); G2: 0
   int m_valid;         // G1: I, G2: H -- weight rows at or beyond are masked
   int R;               // permuted rows (T*k)
   int stages;          // shared-memory pipeline depth
+  int nslots;          // TMEM accumulator slots (per tile; FP8: per 128-K block)
   uint32_t tmem_cols;  // allocated TMEM columns (power of two)
   // G1 epilogue: act [R, I] (f32 / bf16 / e4m3) and FP8 group scales [R, I/128]
   void* act;
   float* act_scale;
   int I;
-  // G2 epilogue: out_acc[t, h] += w[f] * y for f = src[row], t = f / k
+  // G2 epilogue: ybuf[row, h] = w[src[row]] * y[row, h] (bf16, f32 for TF32)
   const int* src;
   const float* topw;
-  float* out_acc;
-  int H, k;
+  void* ybuf;
+  int H;
   // FP8: weight block scales and activation group scales [R, kblocks]
   const float* w_scale;
   int w_scale_rows_per_e;  // G1: 2I/128, G2: H/128
@@ -43,15 +47,17 @@ struct GemmArgs {
 };
 
 // smem bytes for one pipeline stage: NA weight tiles of 128 rows x 128 B
-// and one token tile of N rows x 128 B
-inline int gemm_stage_bytes(int na, int N) { return na * 16384 + N * 128; }
+// and one token tile of n_max rows x 128 B
+inline int gemm_stage_bytes(int na, int n_max) { return na * 16384 + n_max * 128; }
 
-// bytes of shared memory outside the stage ring
-inline int gemm_extra_smem(int N, int kblocks) {
-  return 1024 /* align slack */ + 256 /* barriers, flags */ + N * kblocks * 4 + 4 * N * 4;
+// bytes of shared memory outside the stage ring (FP8 column scales and the
+// per-column amax exchange are only carved out for FP8 launches)
+inline int gemm_extra_smem(int na, int n_max, int kblocks, bool fp8) {
+  return 1024 /* align slack */ + 512 /* barriers, flags */ +
+         (fp8 ? na * n_max * kblocks * 4 + 4 * n_max * 4 : 0);
 }
 
-// Launch grouped GEMM `g` (1: gate+up with SiLU, 2: down with combine).
+// Launch grouped GEMM `g` (1: gate+up with SiLU, 2: down with weighting).
 cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const CUtensorMap& ta,
                                 const CUtensorMap& tb, int grid, int smem_bytes,
                                 cudaStream_t stream);

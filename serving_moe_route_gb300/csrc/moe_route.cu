@@ -9,11 +9,11 @@
 //   scan_kernel     a-2/a-3: per-expert totals, exclusive scans, per-CTA
 //                   bases and the token-tile work list (single CTA)
 //   gather_kernel   a-2: slot of every pick, src/pos, permuted activation
-//                   rows (FP8: quantised per 128-column group), zeroes the
-//                   fp32 combine accumulator
+//                   rows (FP8: quantised per 128-column group)
 //   grouped GEMM 1  a-4/a-5 (grouped_gemm.cu)
-//   grouped GEMM 2  a-6/a-7 (grouped_gemm.cu)
-//   cast_kernel     fp32 accumulator -> bf16 output (not for f32 layers)
+//   grouped GEMM 2  a-6/a-7: weighted expert rows w[t,j] * y (grouped_gemm.cu)
+//   combine_kernel  a-7: out[t] = sum over j of the token's k weighted rows,
+//                   in pick order (fp32 sum, deterministic)
 // No atomics are used to count or place rows: every slot follows from
 // counts and ranks computed without them.
 #include <cuda.h>
@@ -200,11 +200,22 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
   return before;
 }
 
+// Token-tile width of an expert with `cnt` rows: the plan's tile (from the
+// rows-per-expert estimate) is the floor; with per_expert set, an expert
+// with more rows gets the smallest of 32 / 64 / 128 that covers them (128
+// for anything larger), so hot experts of concentrated routing read each
+// weight block once per 128 rows instead of once per `tile_n` rows.
+__device__ __forceinline__ int expert_tile(int cnt, int tile_n, int per_expert) {
+  if (!per_expert) return tile_n;
+  int n = cnt <= 16 ? 16 : cnt <= 32 ? 32 : cnt <= 64 ? 64 : 128;
+  return n > tile_n ? n : tile_n;
+}
+
 __global__ void __launch_bounds__(1024)
     scan_kernel(const int* __restrict__ chunk_counts, int n_chunks, int E, int tile_n,
-                int max_tiles, int* __restrict__ chunk_base, int* __restrict__ counts,
-                int* __restrict__ offsets, int4* __restrict__ tiles, int* __restrict__ ntiles,
-                unsigned* __restrict__ err) {
+                int per_expert, int max_tiles, int* __restrict__ chunk_base,
+                int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ tiles,
+                int* __restrict__ ntiles, unsigned* __restrict__ err) {
   __shared__ int warp_sums[32];
   __shared__ int tot_rows, tot_tiles;
   const int e = threadIdx.x;
@@ -217,7 +228,8 @@ __global__ void __launch_bounds__(1024)
     }
     counts[e] = cnt;
   }
-  const int ntl = (cnt + tile_n - 1) / tile_n;
+  const int ne = expert_tile(cnt, tile_n, per_expert);
+  const int ntl = (cnt + ne - 1) / ne;
   const int off = block_exclusive_scan(cnt, warp_sums, &tot_rows);
   const int tstart = block_exclusive_scan(ntl, warp_sums, &tot_tiles);
   if (e < E) offsets[e] = off;
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(1024)
   }
   if (e < E) {
     for (int i = 0; i < ntl && tstart + i < max_tiles; ++i)
-      tiles[tstart + i] = make_int4(e, off + i * tile_n, min(tile_n, cnt - i * tile_n), 0);
+      tiles[tstart + i] = make_int4(e, off + i * ne, min(ne, cnt - i * ne), ne);
   }
 }
 
@@ -242,20 +254,10 @@ __global__ void __launch_bounds__(256)
                   const int* __restrict__ lrank, const int* __restrict__ chunk_base,
                   const int* __restrict__ offsets, int T, int H, int E, int k, int tpc,
                   int* __restrict__ src, int* __restrict__ pos, void* __restrict__ xq,
-                  float* __restrict__ xs, float* __restrict__ acc, long long acc_elems) {
+                  float* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
   const long long R = static_cast<long long>(T) * k;
   const long long f = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-
-  // zero the fp32 combine accumulator (grid-stride, float4)
-  {
-    float4* a4 = reinterpret_cast<float4*>(acc);
-    const long long n4 = acc_elems >> 2;
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-         i += stride)
-      a4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
   if (f >= R) return;
   const int e = ids[f];
   if (e < 0) {
@@ -309,20 +311,58 @@ __global__ void __launch_bounds__(256)
 }
 
 // ------------------------------------------------------------------ output
-__global__ void __launch_bounds__(256)
-    cast_kernel(const float* __restrict__ acc, __nv_bfloat16* __restrict__ out, long long n) {
-  const long long n4 = n >> 2;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4;
-       i += stride) {
-    const float4 v = reinterpret_cast<const float4*>(acc)[i];
-    __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
-    __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
-    uint2 o;
-    o.x = *reinterpret_cast<uint32_t*>(&a);
-    o.y = *reinterpret_cast<uint32_t*>(&b);
-    reinterpret_cast<uint2*>(out)[i] = o;
+// a-7: out[t, h] = sum over j = 0..k-1 of ybuf[pos[t*k + j], h], where the
+// rows already carry the routing weight.  One warp per (token, 256 columns),
+// 8 columns per lane, fp32 sum in pick order; skipped picks (pos < 0) add
+// nothing.
+__device__ __forceinline__ void load8(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 r = __ldg(reinterpret_cast<const uint4*>(p));
+  const __nv_bfloat162* b = reinterpret_cast<const __nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __low2float(b[i]);
+    v[2 * i + 1] = __high2float(b[i]);
   }
+}
+__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 r;
+  __nv_bfloat162* b = reinterpret_cast<__nv_bfloat162*>(&r);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) b[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+  *reinterpret_cast<uint4*>(p) = r;
+}
+__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
+  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
+  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+template <typename YT>
+__global__ void __launch_bounds__(256)
+    combine_kernel(const YT* __restrict__ ybuf, const int* __restrict__ pos, int T, int H, int k,
+                   YT* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int chunks = (H + 255) / 256;
+  const long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (g >= static_cast<long long>(T) * chunks) return;
+  const int t = static_cast<int>(g / chunks);
+  const int h0 = static_cast<int>(g % chunks) * 256 + lane * 8;
+  if (h0 >= H) return;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int j = 0; j < k; ++j) {
+    const int p = __ldg(pos + static_cast<size_t>(t) * k + j);
+    if (p < 0) continue;
+    float v[8];
+    load8(ybuf + static_cast<size_t>(p) * H + h0, v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += v[i];
+  }
+  store8(out + static_cast<size_t>(t) * H + h0, acc);
 }
 
 // ------------------------------------------------------------------ host helpers
@@ -401,15 +441,24 @@ static int sm_count() {
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-static int max_stages(int na, int N, int kblocks) {
-  const int budget = 227 * 1024 - gemm_extra_smem(N, kblocks);
-  int s = budget / gemm_stage_bytes(na, N);
+static int max_stages(int na, int n_max, int kblocks, bool fp8) {
+  const int budget = 227 * 1024 - gemm_extra_smem(na, n_max, kblocks, fp8);
+  int s = budget / gemm_stage_bytes(na, n_max);
   return s > 8 ? 8 : s;
 }
 
-static uint32_t tmem_cols_for(int na, int N) {
-  uint32_t need = static_cast<uint32_t>(2 * na * N), c = 32;
-  while (c < need) c <<= 1;
+// TMEM accumulator slots: two per-tile accumulators (double buffer) for
+// BF16/TF32; for FP8 one slot per 128-K block, as many as 512 columns hold
+// (up to 16), so the MMAs can run ahead of the scale-folding epilogue.
+static int slots_for(int na, int n_max, bool fp8) {
+  if (!fp8) return 2;
+  int s = 512 / (na * n_max);
+  return s > 16 ? 16 : s;
+}
+
+static uint32_t tmem_cols_for(int need) {
+  uint32_t c = 32;
+  while (c < static_cast<uint32_t>(need)) c <<= 1;
   return c;
 }
 
@@ -422,13 +471,12 @@ static int plan_ok(const moe_plan_t* p) {
 static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, const int* ids_in,
                         const float* w_in, const void* w13, const float* s13, const void* w2,
                         const float* s2, void* out, void* ws, size_t ws_bytes, void* stream,
-                        void* const* events = nullptr) {
+                        void* const* events = nullptr, bool with_ids = false) {
   if (!plan_ok(p)) return MOE_ERR_INVALID_ARG;
   const bool fp8 = p->dtype == MOE_DTYPE_FP8_BLOCK128;
   if (p->T == 0) return MOE_OK;  // empty batch: nothing to read or write
   if (!x || !w13 || !w2 || !out || !ws) return MOE_ERR_INVALID_ARG;
-  if (!ids_in && !logits) return MOE_ERR_INVALID_ARG;
-  if (ids_in && !w_in) return MOE_ERR_INVALID_ARG;
+  if (with_ids ? (!ids_in || !w_in) : !logits) return MOE_ERR_INVALID_ARG;
   if (fp8 != (s13 != nullptr) || fp8 != (s2 != nullptr)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(w13) || !aligned16(w2) || !aligned16(out) || !aligned16(ws))
     return MOE_ERR_INVALID_ARG;
@@ -453,8 +501,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   float* xs = static_cast<float*>(at(p->off_xs));
   void* act = at(p->off_act);
   float* as = static_cast<float*>(at(p->off_as));
-  float* acc = p->dtype == MOE_DTYPE_F32 ? static_cast<float*>(out)
-                                         : static_cast<float*>(at(p->off_acc));
+  void* ybuf = at(p->off_y);
 
   const int T = p->T, H = p->H, I = p->I, E = p->E, k = p->k;
   const long long R = static_cast<long long>(T) * k;
@@ -466,7 +513,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
 
   // a-1 routing (+ histogram)
   const size_t route_smem = static_cast<size_t>(p->route_tpc) * k * sizeof(int);
-  const int mode = ids_in ? 2 : 1;
+  const int mode = with_ids ? 2 : 1;
   if (p->dtype == MOE_DTYPE_F32)
     launch_route_t<float>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
                           static_cast<const float*>(logits), T, E, k, p->scoring, p->renorm,
@@ -478,21 +525,21 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
                                   chunk_counts, lrank, err);
   mark(1);
   // a-2 / a-3 scan and tile list
-  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, E, p->tile_n, p->max_tiles,
-                                  chunk_base, counts, offsets, tiles, ntiles, err);
+  const int per_expert = fp8 ? 0 : 1;
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, E, p->tile_n, per_expert,
+                                  p->max_tiles, chunk_base, counts, offsets, tiles, ntiles, err);
   mark(2);
   // a-2 gather
-  const long long acc_elems = static_cast<long long>(T) * H;
   const unsigned gblocks = static_cast<unsigned>((R * 32 + 255) / 256);
   if (p->dtype == MOE_DTYPE_F32)
     gather_kernel<0><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
-                                              p->route_tpc, src, pos, xq, xs, acc, acc_elems);
+                                              p->route_tpc, src, pos, xq, xs);
   else if (p->dtype == MOE_DTYPE_BF16)
     gather_kernel<1><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
-                                              p->route_tpc, src, pos, xq, xs, acc, acc_elems);
+                                              p->route_tpc, src, pos, xq, xs);
   else
     gather_kernel<2><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
-                                              p->route_tpc, src, pos, xq, xs, acc, acc_elems);
+                                              p->route_tpc, src, pos, xq, xs);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
 
@@ -503,12 +550,13 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  const int N = p->tile_n;
+  // the largest tile the device may choose: 128 with per-expert widths
+  const int NM = per_expert ? 128 : p->tile_n;
   CUtensorMap ta1, tb1, ta2, tb2;
   if (!make_tmap(&ta1, w13, dt, esize, H, static_cast<uint64_t>(E) * 2 * I, 128) ||
-      !make_tmap(&tb1, xq, dt, esize, H, R, N) ||
+      !make_tmap(&tb1, xq, dt, esize, H, R, kTokBox) ||
       !make_tmap(&ta2, w2, dt, esize, I, static_cast<uint64_t>(E) * H, 128) ||
-      !make_tmap(&tb2, act, dt, esize, I, R, N))
+      !make_tmap(&tb2, act, dt, esize, I, R, kTokBox))
     return MOE_ERR_CUDA;
 
   const int sms = sm_count();
@@ -516,14 +564,13 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   GemmArgs g{};
   g.tiles = tiles;
   g.ntiles = ntiles;
-  g.N = N;
+  g.n_max = NM;
   g.R = static_cast<int>(R);
   g.I = I;
   g.H = H;
-  g.k = k;
   g.src = src;
   g.topw = topw;
-  g.out_acc = acc;
+  g.ybuf = ybuf;
   g.err = err;
   g.limit_ns = kWaitLimitNs;
 
@@ -533,8 +580,9 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   g.a_rows_per_e = 2 * I;
   g.a_up_off = I;
   g.m_valid = I;
-  g.stages = max_stages(2, N, g.kblocks);
-  g.tmem_cols = tmem_cols_for(2, N);
+  g.stages = max_stages(2, NM, g.kblocks, fp8);
+  g.nslots = slots_for(2, NM, fp8);
+  g.tmem_cols = tmem_cols_for(g.nslots * 2 * NM);
   g.act = act;
   g.act_scale = as;
   g.w_scale = s13;
@@ -542,36 +590,39 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   g.b_scale = xs;
   long long work1 = static_cast<long long>(p->max_tiles) * g.mblocks;
   int grid1 = static_cast<int>(work1 < sms ? work1 : sms);
-  int smem1 = g.stages * gemm_stage_bytes(2, N) + gemm_extra_smem(N, g.kblocks);
+  int smem1 = g.stages * gemm_stage_bytes(2, NM) + gemm_extra_smem(2, NM, g.kblocks, fp8);
   if (launch_grouped_gemm(kind, 1, g, ta1, tb1, grid1, smem1, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(4);
 
-  // G2: down, weighted combine
+  // G2: down, routing weight
   g.mblocks = p->g2_mblocks;
   g.kblocks = I / (128 / esize);
   g.a_rows_per_e = H;
   g.a_up_off = 0;
   g.m_valid = H;
-  g.stages = max_stages(1, N, g.kblocks);
-  g.tmem_cols = tmem_cols_for(1, N);
+  g.stages = max_stages(1, NM, g.kblocks, fp8);
+  g.nslots = slots_for(1, NM, fp8);
+  g.tmem_cols = tmem_cols_for(g.nslots * NM);
   g.w_scale = s2;
   g.w_scale_rows_per_e = fp8 ? H / 128 : 0;
   g.b_scale = as;
   long long work2 = static_cast<long long>(p->max_tiles) * g.mblocks;
   int grid2 = static_cast<int>(work2 < sms ? work2 : sms);
-  int smem2 = g.stages * gemm_stage_bytes(1, N) + gemm_extra_smem(N, g.kblocks);
+  int smem2 = g.stages * gemm_stage_bytes(1, NM) + gemm_extra_smem(1, NM, g.kblocks, fp8);
   if (launch_grouped_gemm(kind, 2, g, ta2, tb2, grid2, smem2, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(5);
 
-  if (p->dtype != MOE_DTYPE_F32) {
-    const long long n = acc_elems;
-    long long blocks = (n / 4 + 255) / 256;
-    if (blocks > 4L * sms) blocks = 4L * sms;
-    cast_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-        acc, static_cast<__nv_bfloat16*>(out), n);
-  }
+  // a-7: sum of each token's k weighted rows
+  const long long cwarps = static_cast<long long>(T) * ((H + 255) / 256);
+  const unsigned cblocks = static_cast<unsigned>((cwarps * 32 + 255) / 256);
+  if (p->dtype == MOE_DTYPE_F32)
+    combine_kernel<float><<<cblocks, 256, 0, st>>>(static_cast<const float*>(ybuf), pos, T, H, k,
+                                                   static_cast<float*>(out));
+  else
+    combine_kernel<__nv_bfloat16><<<cblocks, 256, 0, st>>>(
+        static_cast<const __nv_bfloat16*>(ybuf), pos, T, H, k, static_cast<__nv_bfloat16*>(out));
   mark(6);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -656,7 +707,7 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   p.off_xs = take(dtype == MOE_DTYPE_FP8_BLOCK128 ? static_cast<uint64_t>(R) * (H / 128) * 4 : 0);
   p.off_act = take(static_cast<uint64_t>(R) * I * ex);
   p.off_as = take(dtype == MOE_DTYPE_FP8_BLOCK128 ? static_cast<uint64_t>(R) * (I / 128) * 4 : 0);
-  p.off_acc = take(dtype == MOE_DTYPE_F32 ? 0 : static_cast<uint64_t>(T) * H * 4);
+  p.off_y = take(static_cast<uint64_t>(R) * H * (dtype == MOE_DTYPE_F32 ? 4 : 2));
   p.workspace_bytes = off;
 
   // 2) then the estimate (H20 article, para. 3) and the tile it selects
@@ -684,7 +735,6 @@ int moe_plan_describe(const moe_plan_t* p, char* buf, size_t n) {
 int moe_forward(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
                 const float* s13, const void* w2, const float* s2, void* out, void* ws,
                 size_t ws_bytes, void* stream) {
-  if (!logits) return MOE_ERR_INVALID_ARG;
   return forward_impl(plan, x, logits, nullptr, nullptr, w13, s13, w2, s2, out, ws, ws_bytes,
                       stream);
 }
@@ -692,7 +742,7 @@ int moe_forward(const moe_plan_t* plan, const void* x, const void* logits, const
 int moe_forward_timed(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
                       const float* s13, const void* w2, const float* s2, void* out, void* ws,
                       size_t ws_bytes, void* stream, void* const* events, int n_events) {
-  if (!logits || !events || n_events != 7) return MOE_ERR_INVALID_ARG;
+  if (!events || n_events != 7) return MOE_ERR_INVALID_ARG;
   for (int i = 0; i < 7; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   return forward_impl(plan, x, logits, nullptr, nullptr, w13, s13, w2, s2, out, ws, ws_bytes,
@@ -702,17 +752,17 @@ int moe_forward_timed(const moe_plan_t* plan, const void* x, const void* logits,
 int moe_forward_with_ids(const moe_plan_t* plan, const void* x, const int32_t* ids,
                          const float* topk_w, const void* w13, const float* s13, const void* w2,
                          const float* s2, void* out, void* ws, size_t ws_bytes, void* stream) {
-  if (!ids || !topk_w) return MOE_ERR_INVALID_ARG;
-  return forward_impl(plan, x, nullptr, ids, topk_w, w13, s13, w2, s2, out, ws, ws_bytes, stream);
+  return forward_impl(plan, x, nullptr, ids, topk_w, w13, s13, w2, s2, out, ws, ws_bytes, stream,
+                      nullptr, true);
 }
 
 int moe_route_topk(const void* logits, int logits_dtype, int T, int E, int k, int scoring,
                    int renorm, int32_t* ids, float* w, void* stream) {
-  if (!logits || !ids || !w) return MOE_ERR_INVALID_ARG;
   if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) return MOE_ERR_INVALID_ARG;
   if (logits_dtype != MOE_LOGITS_F32 && logits_dtype != MOE_LOGITS_BF16) return MOE_ERR_INVALID_ARG;
   if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return MOE_OK;
+  if (T == 0) return MOE_OK;  // empty batch: null pointers allowed
+  if (!logits || !ids || !w) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int tpc = 8;
   dim3 grid((T + tpc - 1) / tpc);

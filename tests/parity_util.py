@@ -50,6 +50,7 @@ def run_gpu(wl, inp, layer=None):
     rc, bits = layer.check(wl.T)
     assert rc == 0, f"device error word {bits:#x}"
     inter = {k: v.cpu().numpy().copy() for k, v in layer.intermediates(wl.T).items()}
+    inter["tile_n"] = layer.plan(wl.T).tile_n
     return out.float().cpu().double().numpy(), inter, layer
 
 
@@ -82,16 +83,21 @@ def check_routing_and_permutation(wl, inp, inter):
     np.testing.assert_array_equal(inter["offsets"], offsets)
     np.testing.assert_array_equal(inter["src"], src)
     np.testing.assert_array_equal(inter["pos"], pos)
-    # the tile list covers every expert's rows exactly once, in expert order
-    p_tile = None
+    # the tile list covers every expert's rows exactly once, in expert order,
+    # each tile at most its width; the width is the plan's tile (from the
+    # estimate) widened per expert to 32/64/128 by its row count (BF16/F32)
     nt = int(inter["ntiles"][0])
     tiles = inter["tiles"][:nt]
     rows = np.zeros(wl.E, np.int64)
-    for e, r0, n, _ in tiles:
-        assert 0 <= e < wl.E and 1 <= n
+    tile_n = int(inter["tile_n"])
+    for e, r0, n, width in tiles:
+        assert 0 <= e < wl.E and 1 <= n <= width
         assert offsets[e] <= r0 and r0 + n <= offsets[e + 1]
+        c = counts[e]
+        want = tile_n if wl.dtype == W.FP8 else max(
+            tile_n, 16 if c <= 16 else 32 if c <= 32 else 64 if c <= 64 else 128)
+        assert width == want, (e, c, width, want)
         rows[e] += n
-        p_tile = n if p_tile is None else max(p_tile, n)
     np.testing.assert_array_equal(rows, counts)
     return ids_ref, w_ref
 

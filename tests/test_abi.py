@@ -44,7 +44,7 @@ def test_header_is_c_and_layout_matches(B, tmp_path):
     src.write_text(
         '#include <stdio.h>\n#include <stddef.h>\n#include "moe_route.h"\n'
         "int main(void){printf(\"%zu %zu %zu %zu\\n\", sizeof(moe_plan_t),"
-        " offsetof(moe_plan_t, workspace_bytes), offsetof(moe_plan_t, off_acc),"
+        " offsetof(moe_plan_t, workspace_bytes), offsetof(moe_plan_t, off_y),"
         " offsetof(moe_plan_t, tile_n)); return 0;}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER),
@@ -52,7 +52,7 @@ def test_header_is_c_and_layout_matches(B, tmp_path):
     vals = [int(v) for v in subprocess.run([str(exe)], capture_output=True, text=True,
                                            check=True).stdout.split()]
     P = B.MoePlan
-    assert vals == [ctypes.sizeof(P), P.workspace_bytes.offset, P.off_acc.offset,
+    assert vals == [ctypes.sizeof(P), P.workspace_bytes.offset, P.off_y.offset,
                     P.tile_n.offset]
 
 
@@ -81,12 +81,12 @@ def test_plan_workspace_layout(B):
     p = B.moe_plan(128, 2048, 768, 128, 8, B.MOE_DTYPE_BF16)
     offs = [p.off_err, p.off_ids, p.off_w, p.off_chunk_counts, p.off_lrank, p.off_counts,
             p.off_offsets, p.off_chunk_base, p.off_src, p.off_pos, p.off_tiles, p.off_ntiles,
-            p.off_xq, p.off_xs, p.off_act, p.off_as, p.off_acc]
+            p.off_xq, p.off_xs, p.off_act, p.off_as, p.off_y]
     assert all(o % 256 == 0 for o in offs)
     assert offs == sorted(offs)
     R = 128 * 8
     assert p.off_act - p.off_xq >= R * 2048 * 2
-    assert p.workspace_bytes - p.off_acc >= 128 * 2048 * 4
+    assert p.workspace_bytes - p.off_y >= 128 * 2048 * 4
     assert "est=8" in p.describe() and "tile_n=16" in p.describe()
 
 

@@ -104,14 +104,14 @@ def test_empty_batch_enqueues_nothing():
     assert out.shape == (0, 256)
 
 
-def test_repeated_calls_are_stable_and_layer_reuses_workspace():
+def test_repeated_calls_are_deterministic():
     wl = W.custom("repeat", T=64, H=256, I=128, E=16, k=4, dtype=W.BF16, seed=36)
     inp = W.make_inputs(wl)
     layer = PU.make_layer(wl, inp)
     a, _, _ = PU.run_gpu(wl, inp, layer)
     b, _, _ = PU.run_gpu(wl, inp, layer)
-    # only the order of the fp32 combine additions may differ between calls
-    np.testing.assert_allclose(a, b, rtol=0, atol=1e-2 * np.abs(a).max())
+    # the combine sums each token's k rows in pick order: bit-identical calls
+    np.testing.assert_array_equal(a, b)
 
 
 def test_with_ids_matches_routed_forward():
@@ -125,7 +125,7 @@ def test_with_ids_matches_routed_forward():
     rc, bits = layer.check(wl.T)
     assert rc == 0 and bits == 0
     o2 = out2.float().cpu().double().numpy()
-    np.testing.assert_allclose(o2, out, rtol=0, atol=1e-2 * np.abs(out).max())
+    np.testing.assert_array_equal(o2, out)
 
 
 def test_with_ids_reports_bad_and_duplicate_ids():

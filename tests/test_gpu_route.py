@@ -42,7 +42,7 @@ def test_route_workloads(name, renorm):
 
 
 @pytest.mark.parametrize("scoring", [0, 1])
-@pytest.mark.parametrize("E,k", [(8, 2), (40, 3), (128, 8), (400, 6), (1024, 32), (33, 33),
+@pytest.mark.parametrize("E,k", [(8, 2), (40, 3), (128, 8), (400, 6), (1024, 32), (33, 32),
                                  (1, 1), (64, 1)])
 def test_route_edge_rows(E, k, scoring):
     g = torch.Generator().manual_seed(E * 100 + k)
@@ -59,6 +59,13 @@ def test_route_edge_rows(E, k, scoring):
         ids = _compare(lg.to(dt), k, scoring, True)
         assert list(ids[0]) == list(range(k))
         assert list(ids[1]) == list(range(k))
+
+
+def test_route_rejects_k_above_32():
+    from serving_moe_route_gb300 import MoeError
+    lg = torch.randn(4, 40, device="cuda")
+    with pytest.raises(MoeError):
+        route_topk(lg, 33)
 
 
 def test_route_empty_and_single_token():
