@@ -205,6 +205,33 @@ int moe_check(const moe_plan_t* plan, void* ws, uint32_t* bits, void* stream);
  * length it wanted, or MOE_ERR_INVALID_ARG. */
 int moe_plan_describe(const moe_plan_t* plan, char* buf, size_t n);
 
+/*
+ * moe_forward_noalloc -- moe_forward for callers that cannot allocate
+ * device memory (code running inside an allocator hook or a memory pool,
+ * plug-ins whose host forbids device allocation after start-up, call sites
+ * that must run in a fixed memory budget).  The pages have no counterpart of
+ * this entry point.
+ *
+ * The workspace is a 16 MiB array inside the library's device image
+ * (reserved on every GPU that loads the library, held until the process
+ * exits); nothing is allocated, by this call or by the library.  Plans whose
+ * workspace_bytes exceed 16 MiB are rejected with MOE_ERR_WORKSPACE before
+ * any launch (for example T=128, H=2048, I=768, E=128, k=8 in bf16 needs
+ * about 10 MB).  The caller still passes inputs and outputs, with the same
+ * layouts, alignment and errors as moe_forward.
+ *
+ * The first call on each device looks up the array's device address
+ * (a synchronous runtime query); make that first call before any stream
+ * capture.  Every call on a device uses the same array and leaves its
+ * contents behind; the call clears what must start at zero itself.  Calls
+ * whose work overlaps on the GPU (other streams, other threads) race on the
+ * array: serialise them.  The device error word lives in that array, so
+ * moe_check is not available for this entry point.
+ */
+int moe_forward_noalloc(const moe_plan_t* plan, const void* x, const void* logits,
+                        const void* w13, const float* s13, const void* w2, const float* s2,
+                        void* out, void* stream);
+
 /* moe_strerror -- static message for a MOE_* return code. */
 const char* moe_strerror(int code);
 

@@ -27,8 +27,9 @@ MOE_DTYPE_F32, MOE_DTYPE_BF16, MOE_DTYPE_FP8_BLOCK128 = 0, 1, 2
 MOE_LOGITS_F32, MOE_LOGITS_BF16 = 0, 1
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 
-EXPORTED = ("moe_plan", "moe_forward", "moe_forward_timed", "moe_forward_with_ids", "moe_route_topk", "moe_check",
-            "moe_plan_describe", "moe_strerror", "moe_abi_version")
+EXPORTED = ("moe_plan", "moe_forward", "moe_forward_timed", "moe_forward_with_ids",
+            "moe_forward_noalloc", "moe_route_topk", "moe_check", "moe_plan_describe",
+            "moe_strerror", "moe_abi_version")
 
 
 class MoePlan(ctypes.Structure):
@@ -90,6 +91,8 @@ def lib() -> ctypes.CDLL:
     L.moe_forward_with_ids.argtypes = [ctypes.POINTER(MoePlan), P, P, P, P, P, P, P, P, P,
                                        ctypes.c_size_t, P]
     L.moe_forward_with_ids.restype = i
+    L.moe_forward_noalloc.argtypes = [ctypes.POINTER(MoePlan), P, P, P, P, P, P, P, P]
+    L.moe_forward_noalloc.restype = i
     L.moe_route_topk.argtypes = [P, i, i, i, i, i, i, P, P, P]
     L.moe_route_topk.restype = i
     L.moe_check.argtypes = [ctypes.POINTER(MoePlan), P, ctypes.POINTER(c_u32), P]
@@ -136,6 +139,12 @@ def moe_forward_timed(plan, x, logits, w13, s13, w2, s2, out, ws, ws_bytes, stre
 def moe_forward_with_ids(plan, x, ids, topk_w, w13, s13, w2, s2, out, ws, ws_bytes, stream):
     return lib().moe_forward_with_ids(ctypes.byref(plan), x, ids, topk_w, w13, s13, w2, s2, out,
                                       ws, ws_bytes, stream)
+
+
+def moe_forward_noalloc(plan, x, logits, w13, s13, w2, s2, out, stream):
+    """moe_forward with the library's built-in 16 MiB device workspace (no
+    allocation anywhere); for callers that cannot allocate device memory."""
+    return lib().moe_forward_noalloc(ctypes.byref(plan), x, logits, w13, s13, w2, s2, out, stream)
 
 
 def moe_route_topk(logits, logits_dtype, T, E, k, scoring, renorm, ids, w, stream):

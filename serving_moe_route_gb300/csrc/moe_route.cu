@@ -792,4 +792,48 @@ int moe_check(const moe_plan_t* plan, void* ws, uint32_t* bits, void* stream) {
   return word ? MOE_ERR_DEVICE : MOE_OK;
 }
 
+// ------------------------------------------------------------------ no-alloc entry
+// Some callers cannot call cudaMalloc at all: code that runs inside a
+// framework's allocator hook or a custom memory pool, plug-ins whose host
+// forbids device allocation after start-up, and call sites that must stay
+// free of allocation so they can be replayed in a fixed memory budget.
+// moe_forward_noalloc serves them with a workspace that lives in this
+// library's own device image: a file-scope array, reserved when the module
+// is loaded on a device and held until the process exits.  Its size is the
+// hard limit of this entry point.
+static constexpr size_t kNoAllocWorkspaceBytes = size_t(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
+
+// Device address of g_noalloc_workspace, looked up once per device.  In host
+// code the array's name is only a host-side stand-in, never a device
+// address, so it must not be passed to a kernel.
+static void* noalloc_workspace_ptr(int dev) {
+  constexpr int kMaxDevices = 64;
+  static void* ptrs[kMaxDevices] = {};
+  static std::mutex mu;
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess) return nullptr;
+    ptrs[dev] = p;
+  }
+  return ptrs[dev];
+}
+
+int moe_forward_noalloc(const moe_plan_t* plan, const void* x, const void* logits,
+                        const void* w13, const float* s13, const void* w2, const float* s2,
+                        void* out, void* stream) {
+  if (!plan_ok(plan)) return MOE_ERR_INVALID_ARG;
+  if (plan->workspace_bytes > kNoAllocWorkspaceBytes) return MOE_ERR_WORKSPACE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  void* ws = noalloc_workspace_ptr(dev);
+  if (!ws) return MOE_ERR_CUDA;
+  // the error word is the only region that must start from zero; the
+  // forward clears it on the stream before its first kernel
+  return forward_impl(plan, x, logits, nullptr, nullptr, w13, s13, w2, s2, out, ws,
+                      kNoAllocWorkspaceBytes, stream);
+}
+
 }  // extern "C"
