@@ -130,7 +130,8 @@ typedef struct moe_plan {
  * sigmoid.  The workspace capacity is fixed first from (T, k, E, H, I,
  * dtype) alone; then est = force_est if force_est > 0, else
  * max(1, ceil(T*k/E)), and tile_n = 16 / 32 / 64 / 128 for est <= 16 /
- * <= 32 / <= 64 / above.
+ * <= 32 / <= 64 / above (FP8: at most 64, the width its scale-folding
+ * epilogue holds in registers).
  * Errors: MOE_ERR_INVALID_ARG (null plan, negative or out-of-range sizes,
  * bad enums), MOE_ERR_UNSUPPORTED (H or I not a multiple of the dtype's
  * K step).

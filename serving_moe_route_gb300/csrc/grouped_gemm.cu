@@ -19,9 +19,12 @@
 //                     k rows of a token are summed by the combine kernel)
 //
 // FP8 [128,128] block scales (Lab notes #6, config file line): each 128-K
-// block is accumulated into its own TMEM slot (up to 16 slots in flight) and
-// the epilogue warps fold it into fp32 registers with the product
-// weight-scale x activation-scale, so arbitrary fp32 scales are honoured.
+// block is accumulated into its own TMEM slot; the slots form two groups
+// (up to 8 blocks each) handed between the MMA warp and the epilogue as a
+// unit, and the epilogue folds every block into fp32 registers with the
+// product weight-scale x activation-scale, so arbitrary fp32 scales are
+// honoured.  FP8 kernels are specialised per tile width (16/32/64; the
+// gate and up register accumulators of a 128-wide tile would not fit).
 //
 // Every wait is bounded (see mbar_wait); a timeout sets MOE_DEVERR_TIMEOUT
 // in the error word, raises a CTA-wide abort flag, drains in-flight copies
@@ -34,9 +37,6 @@
 
 namespace moe {
 
-constexpr int kThreads = 320;
-constexpr int kEpiThreads = 256;
-constexpr int kMaxHalf = 64;  // columns per epilogue thread at n = 128
 constexpr int kMaxSlots = 16;
 constexpr unsigned kDevErrTimeout = 4u;
 
@@ -58,6 +58,10 @@ struct KindTraits<KIND_E4M3> {
   static constexpr int esize = 1;
 };
 
+// 8 epilogue warps: two column halves per TMEM lane quadrant
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = 64 + 32 * kEpiWarps;
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
 // activation (G1 output) and weighted expert output (G2 output) stores
@@ -69,19 +73,27 @@ __device__ __forceinline__ void store_val(void* base, size_t idx, float v) {
     static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
 }
 
-template <int KIND, int G>
+// NT = 0: runtime tile width per work item (BF16/TF32, per-expert widths);
+// NT > 0: fixed width (FP8, the plan's tile)
+template <int KIND, int G, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
                         const __grid_constant__ CUtensorMap tma_b, const GemmArgs args) {
   constexpr int NA = (G == 1) ? 2 : 1;  // G1 multiplies gate and up tiles
   constexpr bool FP8 = (KIND == KIND_E4M3);
+  static_assert(!FP8 || NT > 0, "FP8 kernels are specialised per tile width");
   constexpr int BKE = 128 / KindTraits<KIND>::esize;  // elements per 128-byte K step
+  constexpr int EPI_THREADS = kEpiWarps * 32;
+  constexpr int CS = kEpiWarps / 4;              // column splits per lane quadrant
+  constexpr int CPT = NT > 0 ? NT / CS : 8;      // FP8 columns per epilogue thread
+  static_assert(NT <= 64, "FP8 register accumulators hold at most 2 x 32 columns");
   extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int S = args.stages;
   const int NS = args.nslots;
+  const int GS = FP8 ? (NS >> 1) : 1;  // FP8: K blocks per handed-over group
   const int NM = args.n_max;
   const uint32_t stage_bytes = NA * 16384u + static_cast<uint32_t>(NM) * 128u;
   const uint32_t slot_cols = static_cast<uint32_t>(NA * NM);
@@ -92,8 +104,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + static_cast<size_t>(S) * stage_bytes);
   uint64_t* empty = full + S;
-  uint64_t* accf = empty + S;     // [NS] accumulator slot written by the MMAs
-  uint64_t* acce = accf + NS;     // [NS] accumulator slot drained by the epilogue
+  uint64_t* accf = empty + S;     // [2 or NS] accumulator (group) written by the MMAs
+  uint64_t* acce = accf + NS;     // [2 or NS] accumulator (group) drained by the epilogue
   uint64_t* done = acce + NS;     // all MMAs of this CTA complete
   uint64_t* epib = done + 1;      // epilogue-internal barrier
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epib + 1);
@@ -108,10 +120,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < NS; ++b) {
       mbar_init(smem_u32(&accf[b]), 1);
-      mbar_init(smem_u32(&acce[b]), kEpiThreads);
+      mbar_init(smem_u32(&acce[b]), EPI_THREADS);
     }
     mbar_init(smem_u32(done), 1);
-    mbar_init(smem_u32(epib), kEpiThreads);
+    mbar_init(smem_u32(epib), EPI_THREADS);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -141,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
         const int4 tile = args.tiles[w / args.mblocks];
         const int mb = w % args.mblocks;
-        const int n = tile.w;
+        const int n = NT > 0 ? NT : tile.w;
         const int a_row = tile.x * args.a_rows_per_e + mb * 128;
         const uint32_t tx = NA * 16384u + static_cast<uint32_t>(n) * 128u;
         for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
@@ -172,37 +184,36 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, tc = 0, kc = 0;
+      uint32_t it = 0, tc = 0, gc = 0;
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
-        const int n = args.tiles[w / args.mblocks].w;
+        const int n = NT > 0 ? NT : args.tiles[w / args.mblocks].w;
         const uint32_t idesc = idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(n));
-        uint32_t dbase = 0;
+        uint32_t dbase = 0, buf = 0;
         if (!FP8) {
-          const uint32_t sl = tc % NS;
-          if (!mbar_wait(smem_u32(&acce[sl]), ((tc / NS) & 1u) ^ 1u, limit, abort_flag)) {
+          buf = tc % NS;
+          if (!mbar_wait(smem_u32(&acce[buf]), ((tc / NS) & 1u) ^ 1u, limit, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          dbase = sl * slot_cols;
+          dbase = buf * slot_cols;
         }
         for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
+          if (FP8 && kb % GS == 0) {  // a new group of K blocks: its slots must be drained
+            buf = gc & 1u;
+            if (!mbar_wait(smem_u32(&acce[buf]), ((gc >> 1) & 1u) ^ 1u, limit, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           if (!mbar_wait(smem_u32(&full[s]), (it / S) & 1u, limit, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          uint32_t sl = 0;
-          if (FP8) {
-            sl = kc % NS;
-            if (!mbar_wait(smem_u32(&acce[sl]), ((kc / NS) & 1u) ^ 1u, limit, abort_flag)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            dbase = sl * slot_cols;
-          }
+          if (FP8) dbase = (buf * GS + static_cast<uint32_t>(kb % GS)) * slot_cols;
           const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * stage_bytes);
 #pragma unroll
           for (int a = 0; a < NA; ++a) {
@@ -215,14 +226,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           mma_commit(smem_u32(&empty[s]));  // frees the stage once read
-          if (FP8) {
-            mma_commit(smem_u32(&accf[sl]));
-            ++kc;
+          if (FP8 && (kb % GS == GS - 1 || kb == args.kblocks - 1)) {
+            mma_commit(smem_u32(&accf[buf]));
+            ++gc;
           }
         }
         if (!ok) break;
         if (!FP8) {
-          mma_commit(smem_u32(&accf[tc % NS]));
+          mma_commit(smem_u32(&accf[buf]));
           ++tc;
         }
       }
@@ -239,10 +250,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;
     const int q = warp & 3;     // TMEM lane quadrant this warp may read
-    const int half = ew >> 2;   // which half of the token columns
+    const int part = ew >> 2;   // which part of the token columns (0 .. CS-1)
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t tc = 0, kc = 0, eb = 0;
+    uint32_t tc = 0, gc = 0, eb = 0;
 
     auto ep_barrier = [&]() -> bool {
       mbar_arrive(smem_u32(epib));
@@ -254,13 +265,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
       const int4 tile = args.tiles[w / args.mblocks];
       const int mb = w % args.mblocks;
-      const int row0 = tile.y, nrows = tile.z, n = tile.w;
-      const int hc = n >> 1;  // columns per thread
-      const int c_begin = half * hc;
+      const int row0 = tile.y, nrows = tile.z;
       const int row = mb * 128 + r_in_tile;  // weight row = output feature
       const bool row_ok = row < args.m_valid;
 
       if constexpr (!FP8) {
+        const int n = tile.w;
+        const int hc = n / CS;  // columns per thread
+        const int c_begin = part * hc;
         const uint32_t sl = tc % NS;
         const bool got = mbar_wait(smem_u32(&accf[sl]), (tc / NS) & 1u, limit, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
@@ -308,16 +320,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // -------- FP8: per-column scale products cs[a][kb][j] = s_w[a][kb] * s_x[j][kb]
         const int kbs = args.kblocks;
+        const int c_begin = part * CPT;
         if (!ep_barrier()) {
           ok = false;
           break;
         }
         const float* sw = args.w_scale +
                           (static_cast<size_t>(tile.x) * args.w_scale_rows_per_e + mb) * kbs;
-        for (int i = ew * 32 + lane; i < NA * kbs * NM; i += kEpiThreads) {
-          const int a = i / (kbs * NM);
-          const int kb = (i / NM) % kbs;
-          const int j = i % NM;
+        for (int i = ew * 32 + lane; i < NA * kbs * NT; i += EPI_THREADS) {
+          const int a = i / (kbs * NT);
+          const int kb = (i / NT) % kbs;
+          const int j = i % NT;
           const float swv = __ldg(sw + static_cast<size_t>(a) * (args.I / 128) * kbs + kb);
           cs[i] = (j < nrows) ? swv * __ldg(args.b_scale + static_cast<size_t>(row0 + j) * kbs + kb)
                               : 0.0f;
@@ -326,66 +339,64 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        float acc0[kMaxHalf], acc1[kMaxHalf];  // acc1 (up) is dead code for G2
+        float acc0[CPT], acc1[NA == 2 ? CPT : 1];
 #pragma unroll
-        for (int c = 0; c < kMaxHalf; ++c) {
-          acc0[c] = 0.0f;
-          acc1[c] = 0.0f;
-        }
-        for (int kb = 0; kb < kbs; ++kb, ++kc) {
-          const uint32_t sl = kc % NS;
-          const bool got = mbar_wait(smem_u32(&accf[sl]), (kc / NS) & 1u, limit, abort_flag);
+        for (int c = 0; c < CPT; ++c) acc0[c] = 0.0f;
+#pragma unroll
+        for (int c = 0; c < (NA == 2 ? CPT : 1); ++c) acc1[c] = 0.0f;
+        for (int kb0 = 0; kb0 < kbs; kb0 += GS, ++gc) {
+          const uint32_t buf = gc & 1u;
+          const bool got = mbar_wait(smem_u32(&accf[buf]), (gc >> 1) & 1u, limit, abort_flag);
           if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t dcol = sl * slot_cols;
-          const float* c0p = cs + kb * NM;
-          const float* c1p = cs + (kbs + kb) * NM;
+          const int kend = kb0 + GS < kbs ? kb0 + GS : kbs;
+          for (int kb = kb0; kb < kend; ++kb) {
+            const uint32_t dcol = (buf * GS + static_cast<uint32_t>(kb - kb0)) * slot_cols;
+            const float* c0p = cs + kb * NT + c_begin;
+            const float* c1p = cs + (kbs + kb) * NT + c_begin;
 #pragma unroll
-          for (int c0 = 0; c0 < kMaxHalf; c0 += 8) {
-            if (c0 < hc) {
-              const int cc = c_begin + c0;
+            for (int c0 = 0; c0 < CPT; c0 += 8) {
               float p0[8], p1[8];
-              tmem_ld8(lane_addr + dcol + cc, p0);
-              if (NA == 2) {
-                tmem_ld8(lane_addr + dcol + NM + cc, p1);
+              tmem_ld8(lane_addr + dcol + c_begin + c0, p0);
+              if constexpr (NA == 2) {
+                tmem_ld8(lane_addr + dcol + NM + c_begin + c0, p1);
                 tmem_wait_ld(p0, p1);
               } else {
                 tmem_wait_ld(p0);
               }
-              const float4 s0a = *reinterpret_cast<const float4*>(c0p + cc);
-              const float4 s0b = *reinterpret_cast<const float4*>(c0p + cc + 4);
+              const float4 s0a = *reinterpret_cast<const float4*>(c0p + c0);
+              const float4 s0b = *reinterpret_cast<const float4*>(c0p + c0 + 4);
               const float s0[8] = {s0a.x, s0a.y, s0a.z, s0a.w, s0b.x, s0b.y, s0b.z, s0b.w};
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) acc0[c0 + jj] = fmaf(p0[jj], s0[jj], acc0[c0 + jj]);
-              if (NA == 2) {
-                const float4 s1a = *reinterpret_cast<const float4*>(c1p + cc);
-                const float4 s1b = *reinterpret_cast<const float4*>(c1p + cc + 4);
+              if constexpr (NA == 2) {
+                const float4 s1a = *reinterpret_cast<const float4*>(c1p + c0);
+                const float4 s1b = *reinterpret_cast<const float4*>(c1p + c0 + 4);
                 const float s1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj) acc1[c0 + jj] = fmaf(p1[jj], s1[jj], acc1[c0 + jj]);
+                for (int jj = 0; jj < 8; ++jj)
+                  acc1[c0 + jj] = fmaf(p1[jj], s1[jj], acc1[c0 + jj]);
               }
             }
           }
           tc_fence_before();
-          mbar_arrive(smem_u32(&acce[sl]));
+          mbar_arrive(smem_u32(&acce[buf]));
         }
         if (!ok) break;
 
         if constexpr (G == 1) {
           // act = SiLU(gate) * up, then e4m3 per token over this 128-row group
 #pragma unroll
-          for (int c = 0; c < kMaxHalf; ++c) {
-            if (c < hc) {
-              acc0[c] = silu_f(acc0[c]) * acc1[c];
-              float m = fabsf(acc0[c]);
+          for (int c = 0; c < CPT; ++c) {
+            acc0[c] = silu_f(acc0[c]) * acc1[c];
+            float m = fabsf(acc0[c]);
 #pragma unroll
-              for (int off = 16; off > 0; off >>= 1)
-                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-              if (lane == 0) red[q * NM + c_begin + c] = m;
-            }
+            for (int off = 16; off > 0; off >>= 1)
+              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+            if (lane == 0) red[q * NT + c_begin + c] = m;
           }
           if (!ep_barrier()) {
             ok = false;
@@ -394,32 +405,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint8_t* act_q = static_cast<uint8_t*>(args.act);
           const int groups = args.I / 128;
 #pragma unroll
-          for (int c = 0; c < kMaxHalf; ++c) {
-            if (c < hc) {
-              const int j = c_begin + c;
-              if (j < nrows) {
-                const float amax =
-                    fmaxf(fmaxf(red[j], red[NM + j]), fmaxf(red[2 * NM + j], red[3 * NM + j]));
-                const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-                float v = __fdiv_rn(acc0[c], scale);
-                v = fmaxf(fminf(v, 448.0f), -448.0f);
-                const size_t slot = static_cast<size_t>(row0 + j);
-                act_q[slot * args.I + row] = static_cast<uint8_t>(
-                    __nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-                if (r_in_tile == 0) args.act_scale[slot * groups + mb] = scale;
-              }
+          for (int c = 0; c < CPT; ++c) {
+            const int j = c_begin + c;
+            if (j < nrows) {
+              const float amax =
+                  fmaxf(fmaxf(red[j], red[NT + j]), fmaxf(red[2 * NT + j], red[3 * NT + j]));
+              const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+              float v = __fdiv_rn(acc0[c], scale);
+              v = fmaxf(fminf(v, 448.0f), -448.0f);
+              const size_t slot = static_cast<size_t>(row0 + j);
+              act_q[slot * args.I + row] =
+                  static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+              if (r_in_tile == 0) args.act_scale[slot * groups + mb] = scale;
             }
           }
         } else {
 #pragma unroll
-          for (int c = 0; c < kMaxHalf; ++c) {
-            if (c < hc) {
-              const int j = c_begin + c;
-              if (j < nrows && row_ok) {
-                const float wt = __ldg(args.topw + __ldg(args.src + row0 + j));
-                store_val<KIND_BF16>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
-                                     wt * acc0[c]);
-              }
+          for (int c = 0; c < CPT; ++c) {
+            const int j = c_begin + c;
+            if (j < nrows && row_ok) {
+              const float wt = __ldg(args.topw + __ldg(args.src + row0 + j));
+              store_val<KIND_BF16>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
+                                   wt * acc0[c]);
             }
           }
         }
@@ -437,10 +444,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, args.tmem_cols);
 }
 
-template <int KIND, int G>
+template <int KIND, int G, int NT>
 static cudaError_t launch_one(const GemmArgs& args, const CUtensorMap& ta, const CUtensorMap& tb,
                               int grid, int smem, cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<KIND, G>;
+  auto kern = grouped_gemm_kernel<KIND, G, NT>;
   static int configured = 0;  // max dynamic smem is a per-function attribute
   if (configured < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -451,19 +458,31 @@ static cudaError_t launch_one(const GemmArgs& args, const CUtensorMap& ta, const
   return cudaGetLastError();
 }
 
+template <int G>
+static cudaError_t launch_fp8(const GemmArgs& args, const CUtensorMap& ta, const CUtensorMap& tb,
+                              int grid, int smem, cudaStream_t stream) {
+  switch (args.n_max) {
+    case 16: return launch_one<KIND_E4M3, G, 16>(args, ta, tb, grid, smem, stream);
+    case 32: return launch_one<KIND_E4M3, G, 32>(args, ta, tb, grid, smem, stream);
+    case 64: return launch_one<KIND_E4M3, G, 64>(args, ta, tb, grid, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
 cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const CUtensorMap& ta,
                                 const CUtensorMap& tb, int grid, int smem, cudaStream_t stream) {
   if (args.nslots < 1 || args.nslots > kMaxSlots) return cudaErrorInvalidValue;
   if (kind == KIND_TF32) {
-    return g == 1 ? launch_one<KIND_TF32, 1>(args, ta, tb, grid, smem, stream)
-                  : launch_one<KIND_TF32, 2>(args, ta, tb, grid, smem, stream);
+    return g == 1 ? launch_one<KIND_TF32, 1, 0>(args, ta, tb, grid, smem, stream)
+                  : launch_one<KIND_TF32, 2, 0>(args, ta, tb, grid, smem, stream);
   }
   if (kind == KIND_BF16) {
-    return g == 1 ? launch_one<KIND_BF16, 1>(args, ta, tb, grid, smem, stream)
-                  : launch_one<KIND_BF16, 2>(args, ta, tb, grid, smem, stream);
+    return g == 1 ? launch_one<KIND_BF16, 1, 0>(args, ta, tb, grid, smem, stream)
+                  : launch_one<KIND_BF16, 2, 0>(args, ta, tb, grid, smem, stream);
   }
-  return g == 1 ? launch_one<KIND_E4M3, 1>(args, ta, tb, grid, smem, stream)
-                : launch_one<KIND_E4M3, 2>(args, ta, tb, grid, smem, stream);
+  if (args.nslots < 2 || (args.nslots & 1)) return cudaErrorInvalidValue;
+  return g == 1 ? launch_fp8<1>(args, ta, tb, grid, smem, stream)
+                : launch_fp8<2>(args, ta, tb, grid, smem, stream);
 }
 
 }  // namespace moe

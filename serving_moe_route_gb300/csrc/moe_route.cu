@@ -9,7 +9,7 @@
 //   scan_kernel     a-2/a-3: per-expert totals, exclusive scans, per-CTA
 //                   bases and the token-tile work list (single CTA)
 //   gather_kernel   a-2: slot of every pick, src/pos, permuted activation
-//                   rows (FP8: quantised per 128-column group)
+//                   rows (FP8: quantised once per token, 128-column groups)
 //   grouped GEMM 1  a-4/a-5 (grouped_gemm.cu)
 //   grouped GEMM 2  a-6/a-7: weighted expert rows w[t,j] * y (grouped_gemm.cu)
 //   combine_kernel  a-7: out[t] = sum over j of the token's k weighted rows,
@@ -246,8 +246,11 @@ __global__ void __launch_bounds__(1024)
 }
 
 // ------------------------------------------------------------------ gather
-// One warp per pick f: its slot, src/pos, and the permuted activation row.
-// XT: input element type; QT: 0 copy f32, 1 copy bf16, 2 quantise bf16 -> e4m3
+// One warp per (token t, 256 columns): the slots of t's k picks (slot =
+// offset[e] + chunk base + rank among equal ids in the routing CTA), src /
+// pos, and t's activation columns copied (FP8: quantised once per token,
+// 128-column groups = 16 lanes x 8 values) into each of the k permuted rows.
+// QT: 0 copy f32, 1 copy bf16, 2 quantise bf16 -> e4m3
 template <int QT>
 __global__ void __launch_bounds__(256)
     gather_kernel(const void* __restrict__ x, const int* __restrict__ ids,
@@ -256,56 +259,89 @@ __global__ void __launch_bounds__(256)
                   int* __restrict__ src, int* __restrict__ pos, void* __restrict__ xq,
                   float* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
-  const long long R = static_cast<long long>(T) * k;
-  const long long f = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-  if (f >= R) return;
-  const int e = ids[f];
-  if (e < 0) {
-    if (lane == 0) pos[f] = -1;
-    return;
+  const int chunks = (H + 255) / 256;
+  const long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  if (g >= static_cast<long long>(T) * chunks) return;
+  const int t = static_cast<int>(g / chunks);
+  const int c = static_cast<int>(g % chunks);
+
+  int my_slot = -1;
+  if (lane < k) {
+    const size_t f = static_cast<size_t>(t) * k + lane;
+    const int e = ids[f];
+    if (e >= 0)
+      my_slot = offsets[e] + chunk_base[static_cast<size_t>(t / tpc) * E + e] + lrank[f];
+    if (c == 0) {
+      pos[f] = my_slot;
+      if (my_slot >= 0) src[my_slot] = static_cast<int>(f);
+    }
   }
-  const int t = static_cast<int>(f / k);
-  const int c = t / tpc;
-  const int slot = offsets[e] + chunk_base[static_cast<size_t>(c) * E + e] + lrank[f];
-  if (lane == 0) {
-    src[slot] = static_cast<int>(f);
-    pos[f] = slot;
-  }
+  const int h0 = c * 256 + lane * 8;
+  const bool active = h0 < H;
   if constexpr (QT == 0) {
-    const float4* xr = reinterpret_cast<const float4*>(static_cast<const float*>(x) +
-                                                       static_cast<size_t>(t) * H);
-    float4* dst = reinterpret_cast<float4*>(static_cast<float*>(xq) + static_cast<size_t>(slot) * H);
-    for (int i = lane; i < H / 4; i += 32) dst[i] = __ldg(xr + i);
+    float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+    const float* xr = static_cast<const float*>(x) + static_cast<size_t>(t) * H + h0;
+    if (active) {
+      v0 = __ldg(reinterpret_cast<const float4*>(xr));
+      v1 = __ldg(reinterpret_cast<const float4*>(xr) + 1);
+    }
+    for (int j = 0; j < k; ++j) {
+      const int s = __shfl_sync(0xffffffffu, my_slot, j);
+      if (s >= 0 && active) {
+        float4* d = reinterpret_cast<float4*>(static_cast<float*>(xq) + static_cast<size_t>(s) * H + h0);
+        d[0] = v0;
+        d[1] = v1;
+      }
+    }
   } else if constexpr (QT == 1) {
-    const uint4* xr = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) +
-                                                     static_cast<size_t>(t) * H);
-    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(xq) +
-                                          static_cast<size_t>(slot) * H);
-    for (int i = lane; i < H / 8; i += 32) dst[i] = __ldg(xr + i);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (active)
+      v = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(x) +
+                                               static_cast<size_t>(t) * H + h0));
+    for (int j = 0; j < k; ++j) {
+      const int s = __shfl_sync(0xffffffffu, my_slot, j);
+      if (s >= 0 && active)
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(xq) + static_cast<size_t>(s) * H +
+                                  h0) = v;
+    }
   } else {
-    // per 128-column group: 4 values per lane
-    const __nv_bfloat16* xr = static_cast<const __nv_bfloat16*>(x) + static_cast<size_t>(t) * H;
-    uint8_t* dst = static_cast<uint8_t*>(xq) + static_cast<size_t>(slot) * H;
-    const int groups = H / 128;
-    for (int g = 0; g < groups; ++g) {
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + g * 128 + lane * 4));
-      const __nv_bfloat162 p0 = *reinterpret_cast<const __nv_bfloat162*>(&raw.x);
-      const __nv_bfloat162 p1 = *reinterpret_cast<const __nv_bfloat162*>(&raw.y);
-      float v[4] = {__low2float(p0), __high2float(p0), __low2float(p1), __high2float(p1)};
-      float m = fmaxf(fmaxf(fabsf(v[0]), fabsf(v[1])), fmaxf(fabsf(v[2]), fabsf(v[3])));
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-      const float scale = __fdiv_rn(fmaxf(m, 1e-10f), 448.0f);
-      uint32_t packed = 0;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (active) {
+      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+          static_cast<const __nv_bfloat16*>(x) + static_cast<size_t>(t) * H + h0));
+      const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        float q = __fdiv_rn(v[i], scale);
-        q = fmaxf(fminf(q, 448.0f), -448.0f);
-        packed |= static_cast<uint32_t>(__nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3))
-                  << (8 * i);
+        v[2 * i] = __low2float(b2[i]);
+        v[2 * i + 1] = __high2float(b2[i]);
       }
-      *reinterpret_cast<uint32_t*>(dst + g * 128 + lane * 4) = packed;
-      if (lane == 0) xs[static_cast<size_t>(slot) * groups + g] = scale;
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1)  // 16 lanes = one 128-column group
+      m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    const float scale = __fdiv_rn(fmaxf(m, 1e-10f), 448.0f);
+    uint2 packed = make_uint2(0u, 0u);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      float q = __fdiv_rn(v[i], scale);
+      q = fmaxf(fminf(q, 448.0f), -448.0f);
+      const uint32_t code = __nv_cvt_float_to_fp8(q, __NV_SATFINITE, __NV_E4M3);
+      if (i < 4)
+        packed.x |= code << (8 * i);
+      else
+        packed.y |= code << (8 * (i - 4));
+    }
+    const int groups = H / 128;
+    for (int j = 0; j < k; ++j) {
+      const int s = __shfl_sync(0xffffffffu, my_slot, j);
+      if (s >= 0 && active) {
+        *reinterpret_cast<uint2*>(static_cast<uint8_t*>(xq) + static_cast<size_t>(s) * H + h0) =
+            packed;
+        if ((lane & 15) == 0) xs[static_cast<size_t>(s) * groups + h0 / 128] = scale;
+      }
     }
   }
 }
@@ -530,7 +566,8 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
                                   p->max_tiles, chunk_base, counts, offsets, tiles, ntiles, err);
   mark(2);
   // a-2 gather
-  const unsigned gblocks = static_cast<unsigned>((R * 32 + 255) / 256);
+  const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
+  const unsigned gblocks = static_cast<unsigned>((gwarps * 32 + 255) / 256);
   if (p->dtype == MOE_DTYPE_F32)
     gather_kernel<0><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
                                               p->route_tpc, src, pos, xq, xs);
@@ -714,6 +751,9 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   const long long est = force_est > 0 ? force_est : (R + E - 1) / E;
   p.est = static_cast<int32_t>(est < 1 ? 1 : est);
   p.tile_n = p.est <= 16 ? 16 : p.est <= 32 ? 32 : p.est <= 64 ? 64 : 128;
+  // FP8: the scale-folding epilogue keeps gate and up sums of each token
+  // column in registers, which caps its tiles at 64 tokens
+  if (dtype == MOE_DTYPE_FP8_BLOCK128 && p.tile_n > 64) p.tile_n = 64;
   *plan = p;
   return MOE_OK;
 }

@@ -69,10 +69,12 @@ def test_plan_estimate_worked_example(B):
 
 @pytest.mark.parametrize("T,est,tile", [(1, 1, 16), (2, 1, 16), (4, 1, 16), (16, 1, 16),
                                         (64, 4, 16), (128, 8, 16), (256, 16, 16),
-                                        (1024, 64, 64), (4096, 256, 128), (512, 32, 32)])
+                                        (1024, 64, 64), (4096, 256, 64), (512, 32, 32)])
 def test_plan_tile_table(B, T, est, tile):
     p = B.moe_plan(T, 2048, 768, 128, 8, B.MOE_DTYPE_FP8_BLOCK128)
     assert p.est == est and p.tile_n == tile
+    pb = B.moe_plan(T, 2048, 768, 128, 8, B.MOE_DTYPE_BF16)  # bf16: no 64 cap
+    assert pb.tile_n == (128 if est > 64 else tile)
     assert p.g1_mblocks == 6 and p.g2_mblocks == 16
     assert p.max_tiles >= -(-T * 8 // 16) + min(128, T * 8)
 

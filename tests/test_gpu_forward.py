@@ -151,3 +151,36 @@ def test_with_ids_reports_bad_and_duplicate_ids():
     assert torch.isfinite(out.float()).all()
     # the context is still healthy: a normal call succeeds afterwards
     PU.run_gpu(wl, inp, layer)
+
+
+def test_forward_in_a_cuda_graph():
+    # the whole forward (its launches and the error-word memset) captures
+    # into one CUDA graph and replays with new inputs in the same buffers
+    wl = W.custom("graph", T=80, H=256, I=128, E=24, k=4, dtype=W.FP8, seed=39)
+    inp = W.make_inputs(wl)
+    inp2 = W.make_activations(W.custom(T=80, H=256, I=128, E=24, k=4, dtype=W.FP8, seed=40))
+    layer = PU.make_layer(wl, inp)
+    dev = layer.device
+    x = inp["x"].to(dev)
+    lg = inp["logits"].to(dev)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    eager1 = layer.forward(x, lg).clone()
+    eager2 = layer.forward(inp2["x"].to(dev), inp2["logits"].to(dev)).clone()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer.forward(x, lg, out)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, lg, out)
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager1)
+    x.copy_(inp2["x"])
+    lg.copy_(inp2["logits"])
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, eager2)
+    rc, bits = layer.check(wl.T)
+    assert rc == 0, bits
