@@ -93,8 +93,11 @@ extern "C" {
  *   src     int32 [T*k]     permuted row -> flat index (expert-major,
  *                           ascending flat index within an expert)
  *   pos     int32 [T*k]     flat index -> permuted row (inverse of src)
- *   tiles   int32 [max_tiles, 4]  {expert, first row, rows, 0} token tiles
+ *   tiles   int32 [max_tiles, 4]  {expert, first row, rows, width} token
+ *                           tiles of grouped GEMM 1, in expert order
  *   ntiles  int32 [1]       number of valid tiles
+ *   tiles2, ntiles2         the same for grouped GEMM 2 when its widths differ
+ *                           (prefill-sized BF16/F32 plans); otherwise unused
  *   err     uint32 [1]      device error word (MOE_DEVERR_* bits)
  *   y       [T*k, H]        routing-weighted expert output per permuted
  *                           row (bf16; f32 for the f32 layer)
@@ -109,7 +112,8 @@ typedef struct moe_plan {
   int32_t force_est;  /* 0, or the caller's override (e.g. T: old estimate) */
   int32_t tile_n;     /* token tile = MMA N (16, 32, 64 or 128) from est; the
                          device widens it per expert for BF16/F32 (an expert
-                         with more rows gets 32 / 64 / 128) */
+                         with more rows gets 32 / 64 / 128, and for grouped
+                         GEMM 2 256 when est > 64) */
   int32_t route_tpc;  /* tokens per routing CTA */
   int32_t n_chunks;   /* routing CTAs = ceil(T / route_tpc) */
   int32_t max_tiles;  /* worst-case token tiles (independent of est) */
@@ -120,7 +124,8 @@ typedef struct moe_plan {
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;
   uint64_t off_xq, off_xs, off_act, off_as, off_y;
-  uint64_t reserved1[4];
+  uint64_t off_tiles2, off_ntiles2;
+  uint64_t reserved1[2];
 } moe_plan_t;
 
 /*

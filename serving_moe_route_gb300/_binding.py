@@ -40,8 +40,9 @@ class MoePlan(ctypes.Structure):
     _fields_ += [(n, c_u64) for n in (
         "workspace_bytes", "off_err", "off_ids", "off_w", "off_chunk_counts", "off_lrank",
         "off_counts", "off_offsets", "off_chunk_base", "off_src", "off_pos", "off_tiles",
-        "off_ntiles", "off_xq", "off_xs", "off_act", "off_as", "off_y")]
-    _fields_ += [("reserved1", c_u64 * 4)]
+        "off_ntiles", "off_xq", "off_xs", "off_act", "off_as", "off_y", "off_tiles2",
+        "off_ntiles2")]
+    _fields_ += [("reserved1", c_u64 * 2)]
 
     def describe(self) -> str:
         buf = ctypes.create_string_buffer(512)

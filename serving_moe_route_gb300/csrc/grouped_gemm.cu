@@ -4,7 +4,7 @@
 // One persistent CTA per SM walks a device-built list of work items
 // (token tile x 128-row weight block).  Swap-AB orientation: the MMA's M
 // side is 128 rows of one expert's weight matrix, its N side a tile of n
-// permuted token rows of that expert, n = 16 .. 128 set per expert from its
+// permuted token rows of that expert, n = 16 .. 256 set per expert from its
 // row count with the rows-per-expert estimate as the floor (H20 article,
 // para. 3), so a decode-sized expert with a handful of rows still fills the
 // 128-wide M side with weights and a hot expert gets wide tiles.
@@ -77,8 +77,7 @@ __device__ __forceinline__ void store_val(void* base, size_t idx, float v) {
 // NT > 0: fixed width (FP8, the plan's tile)
 template <int KIND, int G, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tma_a,
-                        const __grid_constant__ CUtensorMap tma_b, const GemmArgs args) {
+    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   constexpr int NA = (G == 1) ? 2 : 1;  // G1 multiplies gate and up tiles
   constexpr bool FP8 = (KIND == KIND_E4M3);
   static_assert(!FP8 || NT > 0, "FP8 kernels are specialised per tile width");
@@ -128,8 +127,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tma_a);
-    prefetch_tmap(&tma_b);
+    prefetch_tmap(&maps.a);
+    for (int i = 0; i < kTokMaps; ++i) prefetch_tmap(&maps.b[i]);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
@@ -156,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = NT > 0 ? NT : tile.w;
         const int a_row = tile.x * args.a_rows_per_e + mb * 128;
         const uint32_t tx = NA * 16384u + static_cast<uint32_t>(n) * 128u;
+        const CUtensorMap* tmb = &maps.b[tok_map_index(n)];  // one box of n token rows
         for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1u) ^ 1u, limit, abort_flag)) {
@@ -166,10 +166,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, tx);
           const int kx = kb * BKE;
-          tma_load_2d(smem_u32(st), &tma_a, fb, kx, a_row, pol_w);
-          if (NA == 2) tma_load_2d(smem_u32(st + 16384), &tma_a, fb, kx, a_row + args.a_up_off, pol_w);
-          for (int b = 0; b < n; b += kTokBox)
-            tma_load_2d(smem_u32(st + NA * 16384 + b * 128), &tma_b, fb, kx, tile.y + b, pol_x);
+          tma_load_2d(smem_u32(st), &maps.a, fb, kx, a_row, pol_w);
+          if (NA == 2) tma_load_2d(smem_u32(st + 16384), &maps.a, fb, kx, a_row + args.a_up_off, pol_w);
+          tma_load_2d(smem_u32(st + NA * 16384), tmb, fb, kx, tile.y, pol_x);
         }
       }
       if (!ok) {
@@ -273,6 +272,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n = tile.w;
         const int hc = n / CS;  // columns per thread
         const int c_begin = part * hc;
+        float* cw = cs;  // G2: routing weight of each token column of this tile
+        if constexpr (G == 2) {
+          if (!ep_barrier()) {  // the previous tile's readers are done
+            ok = false;
+            break;
+          }
+          for (int j = ew * 32 + lane; j < n; j += EPI_THREADS)
+            cw[j] = (j < nrows) ? __ldg(args.topw + __ldg(args.src + row0 + j)) : 0.0f;
+          if (!ep_barrier()) {
+            ok = false;
+            break;
+          }
+        }
         const uint32_t sl = tc % NS;
         const bool got = mbar_wait(smem_u32(&accf[sl]), (tc / NS) & 1u, limit, abort_flag);
         if (!__all_sync(0xffffffffu, got)) {
@@ -305,11 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) {
                 const int j = cc + jj;
-                if (j < nrows) {
-                  const float wt = __ldg(args.topw + __ldg(args.src + row0 + j));
+                if (j < nrows)
                   store_val<KIND>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
-                                  wt * yv[jj]);
-                }
+                                  cw[j] * yv[jj]);
               }
             }
           }
@@ -445,8 +455,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int KIND, int G, int NT>
-static cudaError_t launch_one(const GemmArgs& args, const CUtensorMap& ta, const CUtensorMap& tb,
-                              int grid, int smem, cudaStream_t stream) {
+static cudaError_t launch_one(const GemmArgs& args, const GemmMaps& maps, int grid, int smem,
+                              cudaStream_t stream) {
   auto kern = grouped_gemm_kernel<KIND, G, NT>;
   static int configured = 0;  // max dynamic smem is a per-function attribute
   if (configured < smem) {
@@ -454,35 +464,35 @@ static cudaError_t launch_one(const GemmArgs& args, const CUtensorMap& ta, const
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<grid, kThreads, smem, stream>>>(ta, tb, args);
+  kern<<<grid, kThreads, smem, stream>>>(maps, args);
   return cudaGetLastError();
 }
 
 template <int G>
-static cudaError_t launch_fp8(const GemmArgs& args, const CUtensorMap& ta, const CUtensorMap& tb,
-                              int grid, int smem, cudaStream_t stream) {
+static cudaError_t launch_fp8(const GemmArgs& args, const GemmMaps& maps, int grid, int smem,
+                              cudaStream_t stream) {
   switch (args.n_max) {
-    case 16: return launch_one<KIND_E4M3, G, 16>(args, ta, tb, grid, smem, stream);
-    case 32: return launch_one<KIND_E4M3, G, 32>(args, ta, tb, grid, smem, stream);
-    case 64: return launch_one<KIND_E4M3, G, 64>(args, ta, tb, grid, smem, stream);
+    case 16: return launch_one<KIND_E4M3, G, 16>(args, maps, grid, smem, stream);
+    case 32: return launch_one<KIND_E4M3, G, 32>(args, maps, grid, smem, stream);
+    case 64: return launch_one<KIND_E4M3, G, 64>(args, maps, grid, smem, stream);
     default: return cudaErrorInvalidValue;
   }
 }
 
-cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const CUtensorMap& ta,
-                                const CUtensorMap& tb, int grid, int smem, cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const GemmMaps& maps,
+                                int grid, int smem, cudaStream_t stream) {
   if (args.nslots < 1 || args.nslots > kMaxSlots) return cudaErrorInvalidValue;
   if (kind == KIND_TF32) {
-    return g == 1 ? launch_one<KIND_TF32, 1, 0>(args, ta, tb, grid, smem, stream)
-                  : launch_one<KIND_TF32, 2, 0>(args, ta, tb, grid, smem, stream);
+    return g == 1 ? launch_one<KIND_TF32, 1, 0>(args, maps, grid, smem, stream)
+                  : launch_one<KIND_TF32, 2, 0>(args, maps, grid, smem, stream);
   }
   if (kind == KIND_BF16) {
-    return g == 1 ? launch_one<KIND_BF16, 1, 0>(args, ta, tb, grid, smem, stream)
-                  : launch_one<KIND_BF16, 2, 0>(args, ta, tb, grid, smem, stream);
+    return g == 1 ? launch_one<KIND_BF16, 1, 0>(args, maps, grid, smem, stream)
+                  : launch_one<KIND_BF16, 2, 0>(args, maps, grid, smem, stream);
   }
   if (args.nslots < 2 || (args.nslots & 1)) return cudaErrorInvalidValue;
-  return g == 1 ? launch_fp8<1>(args, ta, tb, grid, smem, stream)
-                : launch_fp8<2>(args, ta, tb, grid, smem, stream);
+  return g == 1 ? launch_fp8<1>(args, maps, grid, smem, stream)
+                : launch_fp8<2>(args, maps, grid, smem, stream);
 }
 
 }  // namespace moe

@@ -10,8 +10,19 @@ namespace moe {
 // operand element kinds of the grouped GEMMs
 enum GemmKind : int { KIND_TF32 = 0, KIND_BF16 = 1, KIND_E4M3 = 2 };
 
-// TMA box height of the token-tile loads: a tile of n rows is n/16 boxes
-constexpr int kTokBox = 16;
+// Tensor maps of one grouped GEMM: the weight operand (128-row boxes) and
+// the permuted token rows with one map per tile height 16, 32, 64, 128, 256,
+// so that every token tile is a single TMA box.
+constexpr int kTokMaps = 5;
+struct GemmMaps {
+  CUtensorMap a;
+  CUtensorMap b[kTokMaps];
+};
+
+// index into GemmMaps::b of a tile n rows high (n a power of two, 16..256)
+__host__ __device__ inline int tok_map_index(int n) {
+  return n <= 16 ? 0 : n <= 32 ? 1 : n <= 64 ? 2 : n <= 128 ? 3 : 4;
+}
 
 // Arguments of one grouped GEMM launch (swap-AB orientation: the MMA's M
 // side is 128 weight rows of one expert, its N side a tile of up to
@@ -50,16 +61,15 @@ struct GemmArgs {
 // and one token tile of n_max rows x 128 B
 inline int gemm_stage_bytes(int na, int n_max) { return na * 16384 + n_max * 128; }
 
-// bytes of shared memory outside the stage ring (FP8 column scales and the
-// per-column amax exchange are only carved out for FP8 launches)
+// bytes of shared memory outside the stage ring (FP8: column scale products
+// and the per-column amax exchange; otherwise G2's per-column weights)
 inline int gemm_extra_smem(int na, int n_max, int kblocks, bool fp8) {
   return 1024 /* align slack */ + 512 /* barriers, flags */ +
-         (fp8 ? na * n_max * kblocks * 4 + 4 * n_max * 4 : 0);
+         (fp8 ? na * n_max * kblocks * 4 + 4 * n_max * 4 : n_max * 4 /* column weights */);
 }
 
 // Launch grouped GEMM `g` (1: gate+up with SiLU, 2: down with weighting).
-cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const CUtensorMap& ta,
-                                const CUtensorMap& tb, int grid, int smem_bytes,
-                                cudaStream_t stream);
+cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const GemmMaps& maps,
+                                int grid, int smem_bytes, cudaStream_t stream);
 
 }  // namespace moe

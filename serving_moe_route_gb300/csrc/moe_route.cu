@@ -202,22 +202,42 @@ __device__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
 
 // Token-tile width of an expert with `cnt` rows: the plan's tile (from the
 // rows-per-expert estimate) is the floor; with per_expert set, an expert
-// with more rows gets the smallest of 32 / 64 / 128 that covers them (128
-// for anything larger), so hot experts of concentrated routing read each
-// weight block once per 128 rows instead of once per `tile_n` rows.
-__device__ __forceinline__ int expert_tile(int cnt, int tile_n, int per_expert) {
+// with more rows gets the smallest of 32 / 64 / 128 / 256 that covers them,
+// capped at n_max (256 for prefill-sized plans, else 128), so hot experts
+// of concentrated routing read each weight block once per n_max rows
+// instead of once per `tile_n` rows.
+__device__ __forceinline__ int expert_tile(int cnt, int tile_n, int per_expert, int n_max) {
   if (!per_expert) return tile_n;
-  int n = cnt <= 16 ? 16 : cnt <= 32 ? 32 : cnt <= 64 ? 64 : 128;
-  return n > tile_n ? n : tile_n;
+  int n = cnt <= 16 ? 16 : cnt <= 32 ? 32 : cnt <= 64 ? 64 : cnt <= 128 ? 128 : 256;
+  n = n > tile_n ? n : tile_n;
+  return n < n_max ? n : n_max;
+}
+
+// Writes one token-tile list per grouped GEMM: list 1 with widths up to
+// n_max1 (GEMM1), list 2 up to n_max2 (GEMM2); when the caps agree list 2
+// is not written and GEMM2 reads list 1.
+__device__ void write_tile_list(int e, int E, int cnt, int off, int ne, int max_tiles,
+                               int* warp_sums, int* tot, int4* tiles, int* ntiles,
+                               unsigned* err) {
+  const int ntl = (cnt + ne - 1) / ne;
+  const int tstart = block_exclusive_scan(ntl, warp_sums, tot);
+  if (e == 0) {
+    if (*tot > max_tiles) atomicOr(err, 8u);
+    *ntiles = min(*tot, max_tiles);
+  }
+  if (e < E)
+    for (int i = 0; i < ntl && tstart + i < max_tiles; ++i)
+      tiles[tstart + i] = make_int4(e, off + i * ne, min(ne, cnt - i * ne), ne);
 }
 
 __global__ void __launch_bounds__(1024)
     scan_kernel(const int* __restrict__ chunk_counts, int n_chunks, int E, int tile_n,
-                int per_expert, int max_tiles, int* __restrict__ chunk_base,
-                int* __restrict__ counts, int* __restrict__ offsets, int4* __restrict__ tiles,
-                int* __restrict__ ntiles, unsigned* __restrict__ err) {
+                int per_expert, int n_max1, int n_max2, int max_tiles,
+                int* __restrict__ chunk_base, int* __restrict__ counts,
+                int* __restrict__ offsets, int4* __restrict__ tiles1, int* __restrict__ ntiles1,
+                int4* __restrict__ tiles2, int* __restrict__ ntiles2, unsigned* __restrict__ err) {
   __shared__ int warp_sums[32];
-  __shared__ int tot_rows, tot_tiles;
+  __shared__ int tot_rows, tot_tiles1, tot_tiles2;
   const int e = threadIdx.x;
   int cnt = 0;
   if (e < E) {
@@ -228,21 +248,14 @@ __global__ void __launch_bounds__(1024)
     }
     counts[e] = cnt;
   }
-  const int ne = expert_tile(cnt, tile_n, per_expert);
-  const int ntl = (cnt + ne - 1) / ne;
   const int off = block_exclusive_scan(cnt, warp_sums, &tot_rows);
-  const int tstart = block_exclusive_scan(ntl, warp_sums, &tot_tiles);
   if (e < E) offsets[e] = off;
-  if (e == 0) {
-    offsets[E] = tot_rows;
-    const int nt = min(tot_tiles, max_tiles);
-    if (tot_tiles > max_tiles) atomicOr(err, 8u);
-    *ntiles = nt;
-  }
-  if (e < E) {
-    for (int i = 0; i < ntl && tstart + i < max_tiles; ++i)
-      tiles[tstart + i] = make_int4(e, off + i * ne, min(ne, cnt - i * ne), ne);
-  }
+  if (e == 0) offsets[E] = tot_rows;
+  write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max1), max_tiles,
+                  warp_sums, &tot_tiles1, tiles1, ntiles1, err);
+  if (n_max2 != n_max1)
+    write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max2), max_tiles,
+                    warp_sums, &tot_tiles2, tiles2, ntiles2, err);
 }
 
 // ------------------------------------------------------------------ gather
@@ -484,11 +497,11 @@ static int max_stages(int na, int n_max, int kblocks, bool fp8) {
 }
 
 // TMEM accumulator slots: two per-tile accumulators (double buffer) for
-// BF16/TF32; for FP8 one slot per 128-K block, as many as 512 columns hold
+// BF16/TF32, one when a tile's accumulators take all 512 columns; for FP8 one slot per 128-K block, as many as 512 columns hold
 // (up to 16), so the MMAs can run ahead of the scale-folding epilogue.
 static int slots_for(int na, int n_max, bool fp8) {
-  if (!fp8) return 2;
   int s = 512 / (na * n_max);
+  if (!fp8) return s >= 2 ? 2 : 1;  // a 2 x 256-column G1 tile fills TMEM alone
   return s > 16 ? 16 : s;
 }
 
@@ -533,6 +546,8 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   int* pos = static_cast<int*>(at(p->off_pos));
   int4* tiles = static_cast<int4*>(at(p->off_tiles));
   int* ntiles = static_cast<int*>(at(p->off_ntiles));
+  int4* tiles2 = static_cast<int4*>(at(p->off_tiles2));
+  int* ntiles2 = static_cast<int*>(at(p->off_ntiles2));
   void* xq = at(p->off_xq);
   float* xs = static_cast<float*>(at(p->off_xs));
   void* act = at(p->off_act);
@@ -562,8 +577,15 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   mark(1);
   // a-2 / a-3 scan and tile list
   const int per_expert = fp8 ? 0 : 1;
-  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, E, p->tile_n, per_expert,
-                                  p->max_tiles, chunk_base, counts, offsets, tiles, ntiles, err);
+  // the largest tile the device may choose per GEMM.  GEMM1 keeps two
+  // 2 x n-column accumulators in TMEM, so 128 is its widest double-buffered
+  // tile; GEMM2 (one accumulator) widens hot experts to 256 tokens in
+  // prefill-sized plans (est > 64).
+  const int NM1 = per_expert ? 128 : p->tile_n;
+  const int NM2 = per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, E, p->tile_n, per_expert, NM1, NM2,
+                                  p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
+                                  tiles2, ntiles2, err);
   mark(2);
   // a-2 gather
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
@@ -587,21 +609,22 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                  : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  // the largest tile the device may choose: 128 with per-expert widths
-  const int NM = per_expert ? 128 : p->tile_n;
-  CUtensorMap ta1, tb1, ta2, tb2;
-  if (!make_tmap(&ta1, w13, dt, esize, H, static_cast<uint64_t>(E) * 2 * I, 128) ||
-      !make_tmap(&tb1, xq, dt, esize, H, R, kTokBox) ||
-      !make_tmap(&ta2, w2, dt, esize, I, static_cast<uint64_t>(E) * H, 128) ||
-      !make_tmap(&tb2, act, dt, esize, I, R, kTokBox))
-    return MOE_ERR_CUDA;
+  GemmMaps m1, m2;
+  bool maps_ok = make_tmap(&m1.a, w13, dt, esize, H, static_cast<uint64_t>(E) * 2 * I, 128) &&
+                 make_tmap(&m2.a, w2, dt, esize, I, static_cast<uint64_t>(E) * H, 128);
+  for (int i = 0; i < kTokMaps && maps_ok; ++i) {  // token boxes 16 .. 256 rows
+    const uint32_t rows = 16u << i;
+    maps_ok = make_tmap(&m1.b[i], xq, dt, esize, H, R, rows) &&
+              make_tmap(&m2.b[i], act, dt, esize, I, R, rows);
+  }
+  if (!maps_ok) return MOE_ERR_CUDA;
 
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
   GemmArgs g{};
   g.tiles = tiles;
   g.ntiles = ntiles;
-  g.n_max = NM;
+  g.n_max = NM1;
   g.R = static_cast<int>(R);
   g.I = I;
   g.H = H;
@@ -617,9 +640,9 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   g.a_rows_per_e = 2 * I;
   g.a_up_off = I;
   g.m_valid = I;
-  g.stages = max_stages(2, NM, g.kblocks, fp8);
-  g.nslots = slots_for(2, NM, fp8);
-  g.tmem_cols = tmem_cols_for(g.nslots * 2 * NM);
+  g.stages = max_stages(2, NM1, g.kblocks, fp8);
+  g.nslots = slots_for(2, NM1, fp8);
+  g.tmem_cols = tmem_cols_for(g.nslots * 2 * NM1);
   g.act = act;
   g.act_scale = as;
   g.w_scale = s13;
@@ -627,27 +650,32 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   g.b_scale = xs;
   long long work1 = static_cast<long long>(p->max_tiles) * g.mblocks;
   int grid1 = static_cast<int>(work1 < sms ? work1 : sms);
-  int smem1 = g.stages * gemm_stage_bytes(2, NM) + gemm_extra_smem(2, NM, g.kblocks, fp8);
-  if (launch_grouped_gemm(kind, 1, g, ta1, tb1, grid1, smem1, st) != cudaSuccess)
+  int smem1 = g.stages * gemm_stage_bytes(2, NM1) + gemm_extra_smem(2, NM1, g.kblocks, fp8);
+  if (launch_grouped_gemm(kind, 1, g, m1, grid1, smem1, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(4);
 
   // G2: down, routing weight
   g.mblocks = p->g2_mblocks;
+  g.n_max = NM2;
+  if (NM2 != NM1) {
+    g.tiles = tiles2;
+    g.ntiles = ntiles2;
+  }
   g.kblocks = I / (128 / esize);
   g.a_rows_per_e = H;
   g.a_up_off = 0;
   g.m_valid = H;
-  g.stages = max_stages(1, NM, g.kblocks, fp8);
-  g.nslots = slots_for(1, NM, fp8);
-  g.tmem_cols = tmem_cols_for(g.nslots * NM);
+  g.stages = max_stages(1, NM2, g.kblocks, fp8);
+  g.nslots = slots_for(1, NM2, fp8);
+  g.tmem_cols = tmem_cols_for(g.nslots * NM2);
   g.w_scale = s2;
   g.w_scale_rows_per_e = fp8 ? H / 128 : 0;
   g.b_scale = as;
   long long work2 = static_cast<long long>(p->max_tiles) * g.mblocks;
   int grid2 = static_cast<int>(work2 < sms ? work2 : sms);
-  int smem2 = g.stages * gemm_stage_bytes(1, NM) + gemm_extra_smem(1, NM, g.kblocks, fp8);
-  if (launch_grouped_gemm(kind, 2, g, ta2, tb2, grid2, smem2, st) != cudaSuccess)
+  int smem2 = g.stages * gemm_stage_bytes(1, NM2) + gemm_extra_smem(1, NM2, g.kblocks, fp8);
+  if (launch_grouped_gemm(kind, 2, g, m2, grid2, smem2, st) != cudaSuccess)
     return MOE_ERR_CUDA;
   mark(5);
 
@@ -740,6 +768,8 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   p.off_pos = take(R * 4);
   p.off_tiles = take(static_cast<uint64_t>(max_tiles) * 16);
   p.off_ntiles = take(16);
+  p.off_tiles2 = take(static_cast<uint64_t>(max_tiles) * 16);
+  p.off_ntiles2 = take(16);
   p.off_xq = take(static_cast<uint64_t>(R) * H * ex);
   p.off_xs = take(dtype == MOE_DTYPE_FP8_BLOCK128 ? static_cast<uint64_t>(R) * (H / 128) * 4 : 0);
   p.off_act = take(static_cast<uint64_t>(R) * I * ex);

@@ -125,6 +125,8 @@ class MoELayer:
             "pos": view(p.off_pos, R, torch.int32),
             "tiles": view(p.off_tiles, p.max_tiles * 4, torch.int32).view(p.max_tiles, 4),
             "ntiles": view(p.off_ntiles, 1, torch.int32),
+            "tiles2": view(p.off_tiles2, p.max_tiles * 4, torch.int32).view(p.max_tiles, 4),
+            "ntiles2": view(p.off_ntiles2, 1, torch.int32),
         }
         if self.dtype == FP8:
             out["xq"] = view(p.off_xq, R * self.H, torch.uint8).view(R, self.H)

@@ -85,20 +85,25 @@ def check_routing_and_permutation(wl, inp, inter):
     np.testing.assert_array_equal(inter["pos"], pos)
     # the tile list covers every expert's rows exactly once, in expert order,
     # each tile at most its width; the width is the plan's tile (from the
-    # estimate) widened per expert to 32/64/128 by its row count (BF16/F32)
-    nt = int(inter["ntiles"][0])
-    tiles = inter["tiles"][:nt]
-    rows = np.zeros(wl.E, np.int64)
+    # estimate) widened per expert to 32/64/128 by its row count (BF16/F32);
+    # GEMM2's list of a prefill-sized plan goes up to 256
     tile_n = int(inter["tile_n"])
-    for e, r0, n, width in tiles:
-        assert 0 <= e < wl.E and 1 <= n <= width
-        assert offsets[e] <= r0 and r0 + n <= offsets[e + 1]
-        c = counts[e]
-        want = tile_n if wl.dtype == W.FP8 else max(
-            tile_n, 16 if c <= 16 else 32 if c <= 32 else 64 if c <= 64 else 128)
-        assert width == want, (e, c, width, want)
-        rows[e] += n
-    np.testing.assert_array_equal(rows, counts)
+    lists = [("tiles", "ntiles", 128)]
+    if wl.dtype != W.FP8 and tile_n >= 128:
+        lists.append(("tiles2", "ntiles2", 256))  # GEMM2's own list, widths up to 256
+    for key, nkey, n_max in lists:
+        nt = int(inter[nkey][0])
+        rows = np.zeros(wl.E, np.int64)
+        for e, r0, n, width in inter[key][:nt]:
+            assert 0 <= e < wl.E and 1 <= n <= width
+            assert offsets[e] <= r0 and r0 + n <= offsets[e + 1]
+            c = counts[e]
+            bucket = 16 if c <= 16 else 32 if c <= 32 else 64 if c <= 64 else 128 if c <= 128 \
+                else 256
+            want = tile_n if wl.dtype == W.FP8 else min(n_max, max(tile_n, bucket))
+            assert width == want, (key, e, c, width, want)
+            rows[e] += n
+        np.testing.assert_array_equal(rows, counts)
     return ids_ref, w_ref
 
 
