@@ -290,8 +290,13 @@ def gemm_roofline(wl, stage_ms, acc, pk):
     from serving_moe_route_gb300 import workloads as W
     g1 = statistics.mean(stage_ms["gemm1"])
     g2 = statistics.mean(stage_ms["gemm2"])
-    name, ms, nbytes = ("gemm1", g1, acc["g1_bytes"]) if g1 >= g2 else ("gemm2", g2, acc["g2_bytes"])
-    flops = acc["flops"] * (2.0 / 3.0 if name == "gemm1" else 1.0 / 3.0)
+    if g2 < 0.02 * g1:  # both GEMMs ran as one launch (shared tile list)
+        name, ms, nbytes, flops = "gemm1+gemm2 fused", g1, acc["g1_bytes"] + acc["g2_bytes"], \
+            acc["flops"]
+    elif g1 >= g2:
+        name, ms, nbytes, flops = "gemm1", g1, acc["g1_bytes"], acc["flops"] * 2.0 / 3.0
+    else:
+        name, ms, nbytes, flops = "gemm2", g2, acc["g2_bytes"], acc["flops"] / 3.0
     t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
     tensor_peak = pk["bf16_tflops"] * (2.0 if wl.dtype == W.FP8 else 1.0)
     if wl.dtype == W.F32:
@@ -301,13 +306,13 @@ def gemm_roofline(wl, stage_ms, acc, pk):
         achieved = nbytes / (ms * 1e-3) / 1e9
         return name, {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                       "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                      "traffic": None, "kernel": f"grouped_gemm_kernel ({name})",
+                      "traffic": None, "kernel": f"moe_gemm_kernel ({name})",
                       "algorithmic_bytes": int(nbytes), "mean_ms": round(ms, 5),
                       "peak_source": pk["source"]}
     achieved = flops / (ms * 1e-3) / 1e12
     return name, {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak,
                   "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4), "traffic": None,
-                  "kernel": f"grouped_gemm_kernel ({name})", "algorithmic_flops": flops,
+                  "kernel": f"moe_gemm_kernel ({name})", "algorithmic_flops": flops,
                   "mean_ms": round(ms, 5), "peak_source": pk["source"] + (
                       " (fp8 = 2x bf16 nominal ratio)" if wl.dtype == W.FP8 else "")}
 

@@ -98,6 +98,8 @@ extern "C" {
  *   ntiles  int32 [1]       number of valid tiles
  *   tiles2, ntiles2         the same for grouped GEMM 2 when its widths differ
  *                           (prefill-sized BF16/F32 plans); otherwise unused
+ *   dep     int32 [max_tiles] finished GEMM1 items per tile (when both GEMMs
+ *                           run as one launch)
  *   err     uint32 [1]      device error word (MOE_DEVERR_* bits)
  *   y       [T*k, H]        routing-weighted expert output per permuted
  *                           row (bf16; f32 for the f32 layer)
@@ -124,8 +126,8 @@ typedef struct moe_plan {
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;
   uint64_t off_xq, off_xs, off_act, off_as, off_y;
-  uint64_t off_tiles2, off_ntiles2;
-  uint64_t reserved1[2];
+  uint64_t off_tiles2, off_ntiles2, off_dep;
+  uint64_t reserved1[1];
 } moe_plan_t;
 
 /*
@@ -167,8 +169,9 @@ int moe_forward(const moe_plan_t* plan, const void* x, const void* logits, const
  * launches, for per-kernel timing without a profiler: events[0] before the
  * routing kernel, [1] after routing, [2] after the scan, [3] after the
  * gather, [4] after grouped GEMM 1, [5] after grouped GEMM 2, [6] after the
- * output cast ([6] directly follows [5] for f32 layers).  n_events must be
- * 7.  Same arguments, errors and results as moe_forward otherwise.
+ * combine.  When both GEMMs run as one launch, [4] follows that launch and
+ * [5] directly follows [4].  n_events must be 7.  Same arguments, errors and
+ * results as moe_forward otherwise.
  */
 int moe_forward_timed(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
                       const float* s13, const void* w2, const float* s2, void* out, void* ws,

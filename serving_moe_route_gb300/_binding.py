@@ -41,8 +41,8 @@ class MoePlan(ctypes.Structure):
         "workspace_bytes", "off_err", "off_ids", "off_w", "off_chunk_counts", "off_lrank",
         "off_counts", "off_offsets", "off_chunk_base", "off_src", "off_pos", "off_tiles",
         "off_ntiles", "off_xq", "off_xs", "off_act", "off_as", "off_y", "off_tiles2",
-        "off_ntiles2")]
-    _fields_ += [("reserved1", c_u64 * 2)]
+        "off_ntiles2", "off_dep")]
+    _fields_ += [("reserved1", c_u64 * 1)]
 
     def describe(self) -> str:
         buf = ctypes.create_string_buffer(512)

@@ -9,14 +9,21 @@
 // para. 3), so a decode-sized expert with a handful of rows still fills the
 // 128-wide M side with weights and a hot expert gets wide tiles.
 //
+// GEMM1 (gate+up, a-4/a-5) and GEMM2 (down, a-6/a-7) run as one launch when
+// they share a tile list: GEMM2 items follow all GEMM1 items in the work
+// list, and a GEMM2 item waits until every GEMM1 item of its token tile has
+// written its activations (a per-tile counter released by the GEMM1
+// epilogue), so CTAs that run out of GEMM1 work start GEMM2 work at once.
+//
 //   warp 0      TMA producer: weight tile(s) + token tile per 128-byte K step
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
 //   warps 2..9  epilogue: tcgen05.ld from TMEM, then
-//                 G1: act = SiLU(gate) * up  (FP8: + per-token 128-group
-//                     e4m3 quantisation, clamp with fminf/fmaxf as in
-//                     PR #39593 "Purpose")
-//                 G2: ybuf[row] = w[t,j] * y  (the combine's weighting; the
-//                     k rows of a token are summed by the combine kernel)
+//                 GEMM1: act = SiLU(gate) * up  (FP8: + per-token 128-group
+//                        e4m3 quantisation, clamp with fminf/fmaxf as in
+//                        PR #39593 "Purpose")
+//                 GEMM2: ybuf[row] = w[t,j] * y  (the combine's weighting;
+//                        the k rows of a token are summed by the combine
+//                        kernel)
 //
 // FP8 [128,128] block scales (Lab notes #6, config file line): each 128-K
 // block is accumulated into its own TMEM slot; the slots form two groups
@@ -26,9 +33,9 @@
 // honoured.  FP8 kernels are specialised per tile width (16/32/64; the
 // gate and up register accumulators of a 128-wide tile would not fit).
 //
-// Every wait is bounded (see mbar_wait); a timeout sets MOE_DEVERR_TIMEOUT
-// in the error word, raises a CTA-wide abort flag, drains in-flight copies
-// and MMAs, frees TMEM and returns.
+// Every wait is bounded (see mbar_wait / wait_counter); a timeout sets
+// MOE_DEVERR_TIMEOUT in the error word, raises a CTA-wide abort flag, drains
+// in-flight copies and MMAs, frees TMEM and returns.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -39,6 +46,8 @@ namespace moe {
 
 constexpr int kMaxSlots = 16;
 constexpr unsigned kDevErrTimeout = 4u;
+constexpr int kEpiWarps = 8;  // two column halves per TMEM lane quadrant
+constexpr int kThreads = 64 + 32 * kEpiWarps;
 
 template <int KIND>
 struct KindTraits;
@@ -58,13 +67,9 @@ struct KindTraits<KIND_E4M3> {
   static constexpr int esize = 1;
 };
 
-// 8 epilogue warps: two column halves per TMEM lane quadrant
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
 
-// activation (G1 output) and weighted expert output (G2 output) stores
+// activation (GEMM1 output) and weighted expert output (GEMM2 output) stores
 template <int KIND>
 __device__ __forceinline__ void store_val(void* base, size_t idx, float v) {
   if constexpr (KIND == KIND_TF32)
@@ -73,19 +78,42 @@ __device__ __forceinline__ void store_val(void* base, size_t idx, float v) {
     static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
 }
 
+// Work item w of a launch: GEMM g (0 or 1), token tile t of that GEMM's
+// list, 128-row weight block mb.
+struct Item {
+  int g, t, mb;
+  int4 tile;
+};
+
+__device__ __forceinline__ Item item_at(const GemmArgs& A, int w, int nwork1) {
+  Item it;
+  if (w < nwork1) {
+    it.g = 0;
+    it.t = w / A.p[0].mblocks;
+    it.mb = w % A.p[0].mblocks;
+  } else {
+    const int v = w - nwork1;
+    it.g = 1;
+    it.t = v / A.p[1].mblocks;
+    it.mb = v % A.p[1].mblocks;
+  }
+  it.tile = A.p[it.g].tiles[it.t];
+  return it;
+}
+
 // NT = 0: runtime tile width per work item (BF16/TF32, per-expert widths);
 // NT > 0: fixed width (FP8, the plan's tile)
-template <int KIND, int G, int NT>
+template <int KIND, int NT>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
-  constexpr int NA = (G == 1) ? 2 : 1;  // G1 multiplies gate and up tiles
+    moe_gemm_kernel(const __grid_constant__ GemmMaps maps1, const __grid_constant__ GemmMaps maps2,
+                    const GemmArgs args) {
   constexpr bool FP8 = (KIND == KIND_E4M3);
   static_assert(!FP8 || NT > 0, "FP8 kernels are specialised per tile width");
+  static_assert(NT <= 64, "FP8 register accumulators hold at most 2 x 32 columns");
   constexpr int BKE = 128 / KindTraits<KIND>::esize;  // elements per 128-byte K step
   constexpr int EPI_THREADS = kEpiWarps * 32;
-  constexpr int CS = kEpiWarps / 4;              // column splits per lane quadrant
-  constexpr int CPT = NT > 0 ? NT / CS : 8;      // FP8 columns per epilogue thread
-  static_assert(NT <= 64, "FP8 register accumulators hold at most 2 x 32 columns");
+  constexpr int CS = kEpiWarps / 4;          // column splits per lane quadrant
+  constexpr int CPT = NT > 0 ? NT / CS : 8;  // FP8 columns per epilogue thread
   extern __shared__ uint8_t smem_raw[];
 
   const int warp = threadIdx.x >> 5;
@@ -94,23 +122,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int NS = args.nslots;
   const int GS = FP8 ? (NS >> 1) : 1;  // FP8: K blocks per handed-over group
   const int NM = args.n_max;
-  const uint32_t stage_bytes = NA * 16384u + static_cast<uint32_t>(NM) * 128u;
-  const uint32_t slot_cols = static_cast<uint32_t>(NA * NM);
+  const int NAM = args.na_max;
+  const uint32_t stage_bytes = NAM * 16384u + static_cast<uint32_t>(NM) * 128u;
+  const uint32_t slot_cols = static_cast<uint32_t>(NAM * NM);
   const uint64_t limit = args.limit_ns;
+  const int kb_max = args.p[0].kblocks > args.p[1].kblocks ? args.p[0].kblocks
+                                                            : args.p[1].kblocks;
 
   // ---- shared memory carve-up (stage ring 1024-aligned for 128B swizzle)
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(stages + static_cast<size_t>(S) * stage_bytes);
   uint64_t* empty = full + S;
-  uint64_t* accf = empty + S;     // [2 or NS] accumulator (group) written by the MMAs
-  uint64_t* acce = accf + NS;     // [2 or NS] accumulator (group) drained by the epilogue
-  uint64_t* done = acce + NS;     // all MMAs of this CTA complete
-  uint64_t* epib = done + 1;      // epilogue-internal barrier
+  uint64_t* accf = empty + S;  // [NS] accumulator (group) written by the MMAs
+  uint64_t* acce = accf + NS;  // [NS] accumulator (group) drained by the epilogue
+  uint64_t* done = acce + NS;  // all MMAs of this CTA complete
+  uint64_t* epib = done + 1;   // epilogue-internal barrier
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epib + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* cs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [NA][kb][NM]
-  float* red = cs + NA * args.kblocks * NM;                                      // [4][NM]
+  float* cs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);
+  float* red = cs + 2 * kb_max * NM;  // FP8: [4][NM] per-column amax per lane quadrant
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -127,8 +158,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    prefetch_tmap(&maps.a);
-    for (int i = 0; i < kTokMaps; ++i) prefetch_tmap(&maps.b[i]);
+    for (int i = 0; i < 2; ++i) {
+      const GemmMaps& M = i ? maps2 : maps1;
+      if (i ? args.run2 : args.run1) {
+        prefetch_tmap(&M.a);
+        for (int j = 0; j < kTokMaps; ++j) prefetch_tmap(&M.b[j]);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
@@ -139,7 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int nwork = (*args.ntiles) * args.mblocks;
+  const int nwork1 = args.run1 ? (*args.p[0].ntiles) * args.p[0].mblocks : 0;
+  const int nwork2 = args.run2 ? (*args.p[1].ntiles) * args.p[1].mblocks : 0;
+  const int nwork = nwork1 + nwork2;
   int never = 0;
   bool ok = true;
 
@@ -150,13 +188,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_x = policy_evict_last();   // token tiles: reused per block
       uint32_t it = 0;
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
-        const int4 tile = args.tiles[w / args.mblocks];
-        const int mb = w % args.mblocks;
-        const int n = NT > 0 ? NT : tile.w;
-        const int a_row = tile.x * args.a_rows_per_e + mb * 128;
-        const uint32_t tx = NA * 16384u + static_cast<uint32_t>(n) * 128u;
-        const CUtensorMap* tmb = &maps.b[tok_map_index(n)];  // one box of n token rows
-        for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
+        const Item I = item_at(args, w, nwork1);
+        const GemmPhase& P = args.p[I.g];
+        const GemmMaps& M = I.g ? maps2 : maps1;
+        const int na = I.g ? 1 : 2;
+        const int n = NT > 0 ? NT : I.tile.w;
+        const int a_row = I.tile.x * P.a_rows_per_e + I.mb * 128;
+        const uint32_t tx = na * 16384u + static_cast<uint32_t>(n) * 128u;
+        const CUtensorMap* tmb = &M.b[tok_map_index(n)];  // one box of n token rows
+        if (I.g == 1 && args.fused) {
+          // this tile's activations are written by GEMM1 items of other CTAs
+          if (!wait_counter(args.dep + I.t, args.p[0].mblocks, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+        }
+        for (int kb = 0; kb < P.kblocks; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1u) ^ 1u, limit, abort_flag)) {
             ok = false;
@@ -166,9 +214,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, tx);
           const int kx = kb * BKE;
-          tma_load_2d(smem_u32(st), &maps.a, fb, kx, a_row, pol_w);
-          if (NA == 2) tma_load_2d(smem_u32(st + 16384), &maps.a, fb, kx, a_row + args.a_up_off, pol_w);
-          tma_load_2d(smem_u32(st + NA * 16384), tmb, fb, kx, tile.y, pol_x);
+          tma_load_2d(smem_u32(st), &M.a, fb, kx, a_row, pol_w);
+          if (na == 2) tma_load_2d(smem_u32(st + 16384), &M.a, fb, kx, a_row + P.a_up_off, pol_w);
+          tma_load_2d(smem_u32(st + NAM * 16384), tmb, fb, kx, I.tile.y, pol_x);
         }
       }
       if (!ok) {
@@ -185,7 +233,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, tc = 0, gc = 0;
       for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
-        const int n = NT > 0 ? NT : args.tiles[w / args.mblocks].w;
+        const Item I = item_at(args, w, nwork1);
+        const int na = I.g ? 1 : 2;
+        const int kbs = args.p[I.g].kblocks;
+        const int n = NT > 0 ? NT : I.tile.w;
         const uint32_t idesc = idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(n));
         uint32_t dbase = 0, buf = 0;
         if (!FP8) {
@@ -197,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           dbase = buf * slot_cols;
         }
-        for (int kb = 0; kb < args.kblocks; ++kb, ++it) {
+        for (int kb = 0; kb < kbs; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (FP8 && kb % GS == 0) {  // a new group of K blocks: its slots must be drained
             buf = gc & 1u;
@@ -214,18 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (FP8) dbase = (buf * GS + static_cast<uint32_t>(kb % GS)) * slot_cols;
           const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * stage_bytes);
-#pragma unroll
-          for (int a = 0; a < NA; ++a) {
+          for (int a = 0; a < na; ++a) {
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
               const uint64_t ad = sdesc_sw128(sa + a * 16384 + ks * 32);
-              const uint64_t bd = sdesc_sw128(sa + NA * 16384 + ks * 32);
+              const uint64_t bd = sdesc_sw128(sa + NAM * 16384 + ks * 32);
               const uint32_t accumulate = FP8 ? (ks != 0) : ((kb | ks) != 0);
               mma_issue<KIND>(tmem_base + dbase + a * NM, ad, bd, idesc, accumulate);
             }
           }
           mma_commit(smem_u32(&empty[s]));  // frees the stage once read
-          if (FP8 && (kb % GS == GS - 1 || kb == args.kblocks - 1)) {
+          if (FP8 && (kb % GS == GS - 1 || kb == kbs - 1)) {
             mma_commit(smem_u32(&accf[buf]));
             ++gc;
           }
@@ -248,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;
-    const int q = warp & 3;     // TMEM lane quadrant this warp may read
-    const int part = ew >> 2;   // which part of the token columns (0 .. CS-1)
+    const int q = warp & 3;    // TMEM lane quadrant this warp may read
+    const int part = ew >> 2;  // which half of the token columns
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     uint32_t tc = 0, gc = 0, eb = 0;
@@ -262,18 +312,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
-      const int4 tile = args.tiles[w / args.mblocks];
-      const int mb = w % args.mblocks;
-      const int row0 = tile.y, nrows = tile.z;
-      const int row = mb * 128 + r_in_tile;  // weight row = output feature
-      const bool row_ok = row < args.m_valid;
+      const Item I = item_at(args, w, nwork1);
+      const GemmPhase& P = args.p[I.g];
+      const int na = I.g ? 1 : 2;
+      const int row0 = I.tile.y, nrows = I.tile.z;
+      const int row = I.mb * 128 + r_in_tile;  // weight row = output feature
+      const bool row_ok = row < P.m_valid;
 
       if constexpr (!FP8) {
-        const int n = tile.w;
+        const int n = I.tile.w;
         const int hc = n / CS;  // columns per thread
         const int c_begin = part * hc;
-        float* cw = cs;  // G2: routing weight of each token column of this tile
-        if constexpr (G == 2) {
+        float* cw = cs;  // GEMM2: routing weight of each token column of this tile
+        if (I.g == 1) {
           if (!ep_barrier()) {  // the previous tile's readers are done
             ok = false;
             break;
@@ -295,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t dcol = sl * slot_cols;
         for (int c0 = 0; c0 < hc; c0 += 8) {
           const int cc = c_begin + c0;
-          if constexpr (G == 1) {
+          if (I.g == 0) {
             float gv[8], uv[8];
             tmem_ld8(lane_addr + dcol + cc, gv);
             tmem_ld8(lane_addr + dcol + NM + cc, uv);
@@ -329,31 +380,42 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++tc;
       } else {
         // -------- FP8: per-column scale products cs[a][kb][j] = s_w[a][kb] * s_x[j][kb]
-        const int kbs = args.kblocks;
+        const int kbs = P.kblocks;
         const int c_begin = part * CPT;
+        if (I.g == 1 && args.fused) {
+          // the activation scales of this tile come from GEMM1 items of
+          // other CTAs in this launch: acquire them (already released)
+          const bool got = wait_counter(args.dep + I.t, args.p[0].mblocks, limit, abort_flag);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            break;
+          }
+        }
         if (!ep_barrier()) {
           ok = false;
           break;
         }
-        const float* sw = args.w_scale +
-                          (static_cast<size_t>(tile.x) * args.w_scale_rows_per_e + mb) * kbs;
-        for (int i = ew * 32 + lane; i < NA * kbs * NT; i += EPI_THREADS) {
+        const float* sw =
+            P.w_scale + (static_cast<size_t>(I.tile.x) * P.w_scale_rows_per_e + I.mb) * kbs;
+        for (int i = ew * 32 + lane; i < na * kbs * NT; i += EPI_THREADS) {
           const int a = i / (kbs * NT);
           const int kb = (i / NT) % kbs;
           const int j = i % NT;
           const float swv = __ldg(sw + static_cast<size_t>(a) * (args.I / 128) * kbs + kb);
-          cs[i] = (j < nrows) ? swv * __ldg(args.b_scale + static_cast<size_t>(row0 + j) * kbs + kb)
+          // L2-coherent load: GEMM2's scales may be written in this launch
+          cs[i] = (j < nrows) ? swv * __ldcg(P.b_scale + static_cast<size_t>(row0 + j) * kbs + kb)
                               : 0.0f;
         }
         if (!ep_barrier()) {
           ok = false;
           break;
         }
-        float acc0[CPT], acc1[NA == 2 ? CPT : 1];
+        float acc0[CPT], acc1[CPT];  // acc1 (up) is only used by GEMM1 items
 #pragma unroll
-        for (int c = 0; c < CPT; ++c) acc0[c] = 0.0f;
-#pragma unroll
-        for (int c = 0; c < (NA == 2 ? CPT : 1); ++c) acc1[c] = 0.0f;
+        for (int c = 0; c < CPT; ++c) {
+          acc0[c] = 0.0f;
+          acc1[c] = 0.0f;
+        }
         for (int kb0 = 0; kb0 < kbs; kb0 += GS, ++gc) {
           const uint32_t buf = gc & 1u;
           const bool got = mbar_wait(smem_u32(&accf[buf]), (gc >> 1) & 1u, limit, abort_flag);
@@ -371,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c0 = 0; c0 < CPT; c0 += 8) {
               float p0[8], p1[8];
               tmem_ld8(lane_addr + dcol + c_begin + c0, p0);
-              if constexpr (NA == 2) {
+              if (na == 2) {
                 tmem_ld8(lane_addr + dcol + NM + c_begin + c0, p1);
                 tmem_wait_ld(p0, p1);
               } else {
@@ -382,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float s0[8] = {s0a.x, s0a.y, s0a.z, s0a.w, s0b.x, s0b.y, s0b.z, s0b.w};
 #pragma unroll
               for (int jj = 0; jj < 8; ++jj) acc0[c0 + jj] = fmaf(p0[jj], s0[jj], acc0[c0 + jj]);
-              if constexpr (NA == 2) {
+              if (na == 2) {
                 const float4 s1a = *reinterpret_cast<const float4*>(c1p + c0);
                 const float4 s1b = *reinterpret_cast<const float4*>(c1p + c0 + 4);
                 const float s1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
@@ -397,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
 
-        if constexpr (G == 1) {
+        if (I.g == 0) {
           // act = SiLU(gate) * up, then e4m3 per token over this 128-row group
 #pragma unroll
           for (int c = 0; c < CPT; ++c) {
@@ -426,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const size_t slot = static_cast<size_t>(row0 + j);
               act_q[slot * args.I + row] =
                   static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-              if (r_in_tile == 0) args.act_scale[slot * groups + mb] = scale;
+              if (r_in_tile == 0) args.act_scale[slot * groups + I.mb] = scale;
             }
           }
         } else {
@@ -441,6 +503,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+
+      if (I.g == 0 && args.fused) {
+        // publish this GEMM1 item: all epilogue threads' activation stores
+        // become visible (to generic and TMA readers) before the count moves
+        fence_proxy_async_global();
+        __threadfence();
+        if (!ep_barrier()) {
+          ok = false;
+          break;
+        }
+        if (ew == 0 && lane == 0) atomicAdd(args.dep + I.t, 1);
+      }
     }
     if (!ok) {
       *abort_flag = 1;
@@ -454,45 +528,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, args.tmem_cols);
 }
 
-template <int KIND, int G, int NT>
-static cudaError_t launch_one(const GemmArgs& args, const GemmMaps& maps, int grid, int smem,
+template <int KIND, int NT>
+static cudaError_t launch_one(const GemmArgs& args, const GemmMaps* maps, int grid, int smem,
                               cudaStream_t stream) {
-  auto kern = grouped_gemm_kernel<KIND, G, NT>;
+  auto kern = moe_gemm_kernel<KIND, NT>;
   static int configured = 0;  // max dynamic smem is a per-function attribute
   if (configured < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<grid, kThreads, smem, stream>>>(maps, args);
+  kern<<<grid, kThreads, smem, stream>>>(maps[0], maps[1], args);
   return cudaGetLastError();
 }
 
-template <int G>
-static cudaError_t launch_fp8(const GemmArgs& args, const GemmMaps& maps, int grid, int smem,
-                              cudaStream_t stream) {
+cudaError_t launch_grouped_gemm(int kind, const GemmArgs& args, const GemmMaps* maps, int grid,
+                                int smem, cudaStream_t stream) {
+  if (args.nslots < 1 || args.nslots > kMaxSlots) return cudaErrorInvalidValue;
+  if (kind == KIND_TF32) return launch_one<KIND_TF32, 0>(args, maps, grid, smem, stream);
+  if (kind == KIND_BF16) return launch_one<KIND_BF16, 0>(args, maps, grid, smem, stream);
+  if (args.nslots < 2 || (args.nslots & 1)) return cudaErrorInvalidValue;
   switch (args.n_max) {
-    case 16: return launch_one<KIND_E4M3, G, 16>(args, maps, grid, smem, stream);
-    case 32: return launch_one<KIND_E4M3, G, 32>(args, maps, grid, smem, stream);
-    case 64: return launch_one<KIND_E4M3, G, 64>(args, maps, grid, smem, stream);
+    case 16: return launch_one<KIND_E4M3, 16>(args, maps, grid, smem, stream);
+    case 32: return launch_one<KIND_E4M3, 32>(args, maps, grid, smem, stream);
+    case 64: return launch_one<KIND_E4M3, 64>(args, maps, grid, smem, stream);
     default: return cudaErrorInvalidValue;
   }
-}
-
-cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const GemmMaps& maps,
-                                int grid, int smem, cudaStream_t stream) {
-  if (args.nslots < 1 || args.nslots > kMaxSlots) return cudaErrorInvalidValue;
-  if (kind == KIND_TF32) {
-    return g == 1 ? launch_one<KIND_TF32, 1, 0>(args, maps, grid, smem, stream)
-                  : launch_one<KIND_TF32, 2, 0>(args, maps, grid, smem, stream);
-  }
-  if (kind == KIND_BF16) {
-    return g == 1 ? launch_one<KIND_BF16, 1, 0>(args, maps, grid, smem, stream)
-                  : launch_one<KIND_BF16, 2, 0>(args, maps, grid, smem, stream);
-  }
-  if (args.nslots < 2 || (args.nslots & 1)) return cudaErrorInvalidValue;
-  return g == 1 ? launch_fp8<1>(args, maps, grid, smem, stream)
-                : launch_fp8<2>(args, maps, grid, smem, stream);
 }
 
 }  // namespace moe

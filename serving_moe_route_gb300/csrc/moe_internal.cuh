@@ -24,52 +24,64 @@ __host__ __device__ inline int tok_map_index(int n) {
   return n <= 16 ? 0 : n <= 32 ? 1 : n <= 64 ? 2 : n <= 128 ? 3 : 4;
 }
 
+// One of the two grouped GEMMs of the layer.
+struct GemmPhase {
+  const int4* tiles;        // [max_tiles] {expert, first permuted row, rows, tile n}
+  const int* ntiles;        // device count of valid tiles
+  int mblocks;              // 128-row weight blocks per expert (G1: ceil(I/128))
+  int kblocks;              // K / (128 bytes / element size)
+  int a_rows_per_e;         // rows of one expert in the A view (G1: 2I, G2: H)
+  int a_up_off;             // G1: I (first up row); G2: 0
+  int m_valid;              // G1: I, G2: H -- weight rows at or beyond are masked
+  const float* w_scale;     // FP8 weight block scales (s13 / s2)
+  int w_scale_rows_per_e;   // G1: 2I/128, G2: H/128
+  const float* b_scale;     // FP8 activation group scales [R, kblocks]
+};
+
 // Arguments of one grouped GEMM launch (swap-AB orientation: the MMA's M
-// side is 128 weight rows of one expert, its N side a tile of up to
-// n_max permuted token rows of that expert; each tile carries its own n).
+// side is 128 weight rows of one expert, its N side a tile of up to n_max
+// permuted token rows of that expert; each tile carries its own n).  A
+// launch runs GEMM1 items, GEMM2 items, or both: fused, GEMM2 items follow
+// GEMM1's in one work list and each waits until all GEMM1 items of its
+// token tile have finished (dep counters).
 struct GemmArgs {
-  const int4* tiles;   // [max_tiles] {expert, first permuted row, rows, tile n}
-  const int* ntiles;   // device count of valid tiles
-  int mblocks;         // 128-row weight blocks per expert (G1: ceil(I/128))
-  int kblocks;         // K / (128 bytes / element size)
+  GemmPhase p[2];      // [0] gate+up GEMM, [1] down GEMM
+  int run1, run2;      // which GEMMs this launch runs
+  int fused;           // both, sharing tile list p[0]; GEMM2 waits on dep
+  int* dep;            // [max_tiles] finished GEMM1 items per tile (fused)
   int n_max;           // largest tile n (stage and TMEM slot size)
-  int a_rows_per_e;    // rows of one expert in the A view (G1: 2I, G2: H)
-  int a_up_off;        // G1: I (first up row); G2: 0
-  int m_valid;         // G1: I, G2: H -- weight rows at or beyond are masked
+  int na_max;          // weight tiles per stage: 2 if GEMM1 runs, else 1
   int R;               // permuted rows (T*k)
   int stages;          // shared-memory pipeline depth
   int nslots;          // TMEM accumulator slots (per tile; FP8: per 128-K block)
   uint32_t tmem_cols;  // allocated TMEM columns (power of two)
-  // G1 epilogue: act [R, I] (f32 / bf16 / e4m3) and FP8 group scales [R, I/128]
+  // GEMM1 output: act [R, I] (f32 / bf16 / e4m3), FP8 group scales [R, I/128]
   void* act;
   float* act_scale;
   int I;
-  // G2 epilogue: ybuf[row, h] = w[src[row]] * y[row, h] (bf16, f32 for TF32)
+  // GEMM2 output: ybuf[row, h] = w[src[row]] * y[row, h] (bf16, f32 for TF32)
   const int* src;
   const float* topw;
   void* ybuf;
   int H;
-  // FP8: weight block scales and activation group scales [R, kblocks]
-  const float* w_scale;
-  int w_scale_rows_per_e;  // G1: 2I/128, G2: H/128
-  const float* b_scale;
   unsigned* err;
   unsigned long long limit_ns;
 };
 
-// smem bytes for one pipeline stage: NA weight tiles of 128 rows x 128 B
+// smem bytes for one pipeline stage: na weight tiles of 128 rows x 128 B
 // and one token tile of n_max rows x 128 B
 inline int gemm_stage_bytes(int na, int n_max) { return na * 16384 + n_max * 128; }
 
 // bytes of shared memory outside the stage ring (FP8: column scale products
-// and the per-column amax exchange; otherwise G2's per-column weights)
-inline int gemm_extra_smem(int na, int n_max, int kblocks, bool fp8) {
+// of the longer K and the per-column amax exchange; otherwise GEMM2's
+// per-column weights)
+inline int gemm_extra_smem(int n_max, int kblocks_max, bool fp8) {
   return 1024 /* align slack */ + 512 /* barriers, flags */ +
-         (fp8 ? na * n_max * kblocks * 4 + 4 * n_max * 4 : n_max * 4 /* column weights */);
+         (fp8 ? 2 * n_max * kblocks_max * 4 + 4 * n_max * 4 : n_max * 4);
 }
 
-// Launch grouped GEMM `g` (1: gate+up with SiLU, 2: down with weighting).
-cudaError_t launch_grouped_gemm(int kind, int g, const GemmArgs& args, const GemmMaps& maps,
-                                int grid, int smem_bytes, cudaStream_t stream);
+// Launch one grouped GEMM kernel (GEMM1, GEMM2 or both fused).
+cudaError_t launch_grouped_gemm(int kind, const GemmArgs& args, const GemmMaps* maps, int grid,
+                                int smem_bytes, cudaStream_t stream);
 
 }  // namespace moe

@@ -10,8 +10,9 @@
 //                   bases and the token-tile work list (single CTA)
 //   gather_kernel   a-2: slot of every pick, src/pos, permuted activation
 //                   rows (FP8: quantised once per token, 128-column groups)
-//   grouped GEMM 1  a-4/a-5 (grouped_gemm.cu)
-//   grouped GEMM 2  a-6/a-7: weighted expert rows w[t,j] * y (grouped_gemm.cu)
+//   grouped GEMMs   a-4/a-5 gate+up with SiLU, a-6/a-7 down with the routing
+//                   weight (grouped_gemm.cu): one launch when both GEMMs share
+//                   a tile list, else one launch each
 //   combine_kernel  a-7: out[t] = sum over j of the token's k weighted rows,
 //                   in pick order (fp32 sum, deterministic)
 // No atomics are used to count or place rows: every slot follows from
@@ -235,8 +236,10 @@ __global__ void __launch_bounds__(1024)
                 int per_expert, int n_max1, int n_max2, int max_tiles,
                 int* __restrict__ chunk_base, int* __restrict__ counts,
                 int* __restrict__ offsets, int4* __restrict__ tiles1, int* __restrict__ ntiles1,
-                int4* __restrict__ tiles2, int* __restrict__ ntiles2, unsigned* __restrict__ err) {
+                int4* __restrict__ tiles2, int* __restrict__ ntiles2, int* __restrict__ dep,
+                unsigned* __restrict__ err) {
   __shared__ int warp_sums[32];
+  for (int i = threadIdx.x; i < max_tiles; i += blockDim.x) dep[i] = 0;  // fused GEMM counters
   __shared__ int tot_rows, tot_tiles1, tot_tiles2;
   const int e = threadIdx.x;
   int cnt = 0;
@@ -491,7 +494,7 @@ static int sm_count() {
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 static int max_stages(int na, int n_max, int kblocks, bool fp8) {
-  const int budget = 227 * 1024 - gemm_extra_smem(na, n_max, kblocks, fp8);
+  const int budget = 227 * 1024 - gemm_extra_smem(n_max, kblocks, fp8);
   int s = budget / gemm_stage_bytes(na, n_max);
   return s > 8 ? 8 : s;
 }
@@ -548,6 +551,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   int* ntiles = static_cast<int*>(at(p->off_ntiles));
   int4* tiles2 = static_cast<int4*>(at(p->off_tiles2));
   int* ntiles2 = static_cast<int*>(at(p->off_ntiles2));
+  int* dep = static_cast<int*>(at(p->off_dep));
   void* xq = at(p->off_xq);
   float* xs = static_cast<float*>(at(p->off_xs));
   void* act = at(p->off_act);
@@ -585,7 +589,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const int NM2 = per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
   scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, E, p->tile_n, per_expert, NM1, NM2,
                                   p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
-                                  tiles2, ntiles2, err);
+                                  tiles2, ntiles2, dep, err);
   mark(2);
   // a-2 gather
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
@@ -621,63 +625,51 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
 
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
+  const int kb1 = H / (128 / esize), kb2 = I / (128 / esize);
+  const int kbmax = kb1 > kb2 ? kb1 : kb2;
   GemmArgs g{};
-  g.tiles = tiles;
-  g.ntiles = ntiles;
-  g.n_max = NM1;
+  g.p[0] = GemmPhase{tiles, ntiles, p->g1_mblocks, kb1, 2 * I, I, I, s13, fp8 ? 2 * I / 128 : 0,
+                     xs};
+  const bool fused = NM1 == NM2;  // one tile list: GEMM2 items follow GEMM1's in one launch
+  g.p[1] = GemmPhase{fused ? tiles : tiles2, fused ? ntiles : ntiles2, p->g2_mblocks, kb2, H, 0,
+                     H, s2, fp8 ? H / 128 : 0, as};
+  g.dep = dep;
   g.R = static_cast<int>(R);
+  g.act = act;
+  g.act_scale = as;
   g.I = I;
-  g.H = H;
   g.src = src;
   g.topw = topw;
   g.ybuf = ybuf;
+  g.H = H;
   g.err = err;
   g.limit_ns = kWaitLimitNs;
-
-  // G1: gate+up, SiLU
-  g.mblocks = p->g1_mblocks;
-  g.kblocks = H / (128 / esize);
-  g.a_rows_per_e = 2 * I;
-  g.a_up_off = I;
-  g.m_valid = I;
-  g.stages = max_stages(2, NM1, g.kblocks, fp8);
-  g.nslots = slots_for(2, NM1, fp8);
-  g.tmem_cols = tmem_cols_for(g.nslots * 2 * NM1);
-  g.act = act;
-  g.act_scale = as;
-  g.w_scale = s13;
-  g.w_scale_rows_per_e = fp8 ? 2 * I / 128 : 0;
-  g.b_scale = xs;
-  long long work1 = static_cast<long long>(p->max_tiles) * g.mblocks;
-  int grid1 = static_cast<int>(work1 < sms ? work1 : sms);
-  int smem1 = g.stages * gemm_stage_bytes(2, NM1) + gemm_extra_smem(2, NM1, g.kblocks, fp8);
-  if (launch_grouped_gemm(kind, 1, g, m1, grid1, smem1, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  mark(4);
-
-  // G2: down, routing weight
-  g.mblocks = p->g2_mblocks;
-  g.n_max = NM2;
-  if (NM2 != NM1) {
-    g.tiles = tiles2;
-    g.ntiles = ntiles2;
+  const GemmMaps maps[2] = {m1, m2};
+  auto launch = [&](int run1, int run2, int nm, int na) -> bool {
+    g.run1 = run1;
+    g.run2 = run2;
+    g.fused = run1 && run2;
+    g.n_max = nm;
+    g.na_max = na;
+    g.stages = max_stages(na, nm, kbmax, fp8);
+    g.nslots = slots_for(na, nm, fp8);
+    g.tmem_cols = tmem_cols_for(g.nslots * na * nm);
+    const long long work = static_cast<long long>(p->max_tiles) *
+                           ((run1 ? p->g1_mblocks : 0) + (run2 ? p->g2_mblocks : 0));
+    const int grid = static_cast<int>(work < sms ? work : sms);
+    const int smem = g.stages * gemm_stage_bytes(na, nm) + gemm_extra_smem(nm, kbmax, fp8);
+    return launch_grouped_gemm(kind, g, maps, grid, smem, st) == cudaSuccess;
+  };
+  if (fused) {
+    if (!launch(1, 1, NM1, 2)) return MOE_ERR_CUDA;
+    mark(4);
+    mark(5);
+  } else {
+    if (!launch(1, 0, NM1, 2)) return MOE_ERR_CUDA;
+    mark(4);
+    if (!launch(0, 1, NM2, 1)) return MOE_ERR_CUDA;
+    mark(5);
   }
-  g.kblocks = I / (128 / esize);
-  g.a_rows_per_e = H;
-  g.a_up_off = 0;
-  g.m_valid = H;
-  g.stages = max_stages(1, NM2, g.kblocks, fp8);
-  g.nslots = slots_for(1, NM2, fp8);
-  g.tmem_cols = tmem_cols_for(g.nslots * NM2);
-  g.w_scale = s2;
-  g.w_scale_rows_per_e = fp8 ? H / 128 : 0;
-  g.b_scale = as;
-  long long work2 = static_cast<long long>(p->max_tiles) * g.mblocks;
-  int grid2 = static_cast<int>(work2 < sms ? work2 : sms);
-  int smem2 = g.stages * gemm_stage_bytes(1, NM2) + gemm_extra_smem(1, NM2, g.kblocks, fp8);
-  if (launch_grouped_gemm(kind, 2, g, m2, grid2, smem2, st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  mark(5);
 
   // a-7: sum of each token's k weighted rows
   const long long cwarps = static_cast<long long>(T) * ((H + 255) / 256);
@@ -770,6 +762,7 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   p.off_ntiles = take(16);
   p.off_tiles2 = take(static_cast<uint64_t>(max_tiles) * 16);
   p.off_ntiles2 = take(16);
+  p.off_dep = take(static_cast<uint64_t>(max_tiles) * 4);
   p.off_xq = take(static_cast<uint64_t>(R) * H * ex);
   p.off_xs = take(dtype == MOE_DTYPE_FP8_BLOCK128 ? static_cast<uint64_t>(R) * (H / 128) * 4 : 0);
   p.off_act = take(static_cast<uint64_t>(R) * I * ex);

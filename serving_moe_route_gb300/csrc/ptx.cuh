@@ -218,3 +218,33 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// ---------------------------------------------------------------- cross-CTA
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// order this thread's generic-proxy global accesses with async-proxy (TMA)
+// accesses to global memory
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *p >= target (another CTA's release), bounded like mbar_wait.
+__device__ __forceinline__ bool wait_counter(const int* p, int target, uint64_t limit_ns,
+                                             volatile int* abort) {
+  if (ld_acquire_gpu(p) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(p) >= target) return true;
+    if (*abort) return false;
+    if (globaltimer() - t0 > limit_ns) return false;
+  }
+}
+
+}  // namespace moe
