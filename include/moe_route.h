@@ -98,8 +98,9 @@ extern "C" {
  *   ntiles  int32 [1]       number of valid tiles
  *   tiles2, ntiles2         the same for grouped GEMM 2 when its widths differ
  *                           (prefill-sized BF16/F32 plans); otherwise unused
- *   dep     int32 [max_tiles] finished GEMM1 items per tile (when both GEMMs
- *                           run as one launch)
+ *   dep     int32 [max_tiles + 2] finished GEMM1 items per tile (when both
+ *                           GEMMs run as one launch), then the work counters
+ *                           of the GEMM launches
  *   err     uint32 [1]      device error word (MOE_DEVERR_* bits)
  *   y       [T*k, H]        routing-weighted expert output per permuted
  *                           row (bf16; f32 for the f32 layer)

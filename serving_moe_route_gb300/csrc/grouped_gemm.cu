@@ -45,6 +45,7 @@
 namespace moe {
 
 constexpr int kMaxSlots = 16;
+constexpr int kQueue = 8;  // work items handed from the producer to MMA + epilogue
 constexpr unsigned kDevErrTimeout = 4u;
 constexpr int kEpiWarps = 8;  // two column halves per TMEM lane quadrant
 constexpr int kThreads = 64 + 32 * kEpiWarps;
@@ -78,6 +79,48 @@ __device__ __forceinline__ void store_val(void* base, size_t idx, float v) {
     static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
 }
 
+// BF16/TF32 epilogue for C token columns starting at cc of one work item:
+// both accumulators are loaded from TMEM before one wait.  GEMM1 writes
+// act = SiLU(gate) * up; GEMM2 writes the weighted rows of one (na = 1) or
+// two (na = 2: rows row and row_b) 128-row weight tiles.
+template <int KIND, int C>
+__device__ __forceinline__ void epi_chunk(const GemmArgs& A, int g, int na, uint32_t taddr, int NM,
+                                          int cc, int row0, int nrows, int row, bool row_ok,
+                                          int row_b, bool row_b_ok, const float* cw) {
+  float v0[C], v1[C];
+  tmem_ld<C>(taddr + cc, v0);
+  if (g == 0 || na == 2) {
+    tmem_ld<C>(taddr + NM + cc, v1);
+    tmem_wait_ld(v0, v1);
+  } else {
+    tmem_wait_ld(v0);
+  }
+  if (g == 0) {
+    if (row_ok) {
+#pragma unroll
+      for (int jj = 0; jj < C; ++jj)
+        if (cc + jj < nrows)
+          store_val<KIND>(A.act, static_cast<size_t>(row0 + cc + jj) * A.I + row,
+                          silu_f(v0[jj]) * v1[jj]);
+    }
+  } else {
+    if (row_ok) {
+#pragma unroll
+      for (int jj = 0; jj < C; ++jj)
+        if (cc + jj < nrows)
+          store_val<KIND>(A.ybuf, static_cast<size_t>(row0 + cc + jj) * A.H + row,
+                          cw[cc + jj] * v0[jj]);
+    }
+    if (na == 2 && row_b_ok) {
+#pragma unroll
+      for (int jj = 0; jj < C; ++jj)
+        if (cc + jj < nrows)
+          store_val<KIND>(A.ybuf, static_cast<size_t>(row0 + cc + jj) * A.H + row_b,
+                          cw[cc + jj] * v1[jj]);
+    }
+  }
+}
+
 // Work item w of a launch: GEMM g (0 or 1), token tile t of that GEMM's
 // list, 128-row weight block mb.
 struct Item {
@@ -102,8 +145,10 @@ __device__ __forceinline__ Item item_at(const GemmArgs& A, int w, int nwork1) {
 }
 
 // NT = 0: runtime tile width per work item (BF16/TF32, per-expert widths);
-// NT > 0: fixed width (FP8, the plan's tile)
-template <int KIND, int NT>
+// NT > 0: fixed width (FP8, the plan's tile).  MODE 1: GEMM1 items only,
+// 2: GEMM2 items only, 3: both (fused); single-GEMM kernels carry only
+// their own epilogue.
+template <int KIND, int NT, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     moe_gemm_kernel(const __grid_constant__ GemmMaps maps1, const __grid_constant__ GemmMaps maps2,
                     const GemmArgs args) {
@@ -138,22 +183,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acce = accf + NS;  // [NS] accumulator (group) drained by the epilogue
   uint64_t* done = acce + NS;  // all MMAs of this CTA complete
   uint64_t* epib = done + 1;   // epilogue-internal barrier
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(epib + 1);
+  uint64_t* qfull = epib + 1;  // [kQueue] work-queue entry written
+  uint64_t* qempty = qfull + kQueue;  // [kQueue] entry read by the MMA thread and the epilogue
+  int* queue = reinterpret_cast<int*>(qempty + kQueue);  // [kQueue] item indices, -1 = end
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(queue + kQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* cs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);
-  float* red = cs + 2 * kb_max * NM;  // FP8: [4][NM] per-column amax per lane quadrant
+  float* cs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 1024);
+  // FP8: [4][NM] per-column amax per lane quadrant (GEMM1), column weights (GEMM2)
+  float* red = cs + 2 * kb_max * NM;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
     }
+    // epilogue-side barriers take one arrival per epilogue warp (lane 0,
+    // after __syncwarp orders the warp's TMEM loads and shared stores)
     for (int b = 0; b < NS; ++b) {
       mbar_init(smem_u32(&accf[b]), 1);
-      mbar_init(smem_u32(&acce[b]), EPI_THREADS);
+      mbar_init(smem_u32(&acce[b]), kEpiWarps);
     }
     mbar_init(smem_u32(done), 1);
-    mbar_init(smem_u32(epib), EPI_THREADS);
+    mbar_init(smem_u32(epib), kEpiWarps);
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(smem_u32(&qfull[i]), 1);
+      mbar_init(smem_u32(&qempty[i]), 1 + kEpiWarps);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -186,17 +241,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_w = policy_evict_first();  // weights: streamed once
       const uint64_t pol_x = policy_evict_last();   // token tiles: reused per block
-      uint32_t it = 0;
-      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
-        const Item I = item_at(args, w, nwork1);
+      uint32_t it = 0, qi = 0;
+      // Fused launches take items in list order from a global counter (CTAs
+      // that finish early take more); the index after the current one is
+      // taken one item ahead so the atomic's latency overlaps the loads.
+      // Single-GEMM launches walk the list with a grid stride.
+      int w_next = MODE == 3 ? atomicAdd(args.work_counter, 1) : static_cast<int>(blockIdx.x);
+      while (ok) {
+        const int w = w_next < nwork ? w_next : -1;
+        if constexpr (MODE == 3) {
+          // hand the item to the MMA thread and the epilogue
+          const int qs = static_cast<int>(qi % kQueue);
+          if (!mbar_wait(smem_u32(&qempty[qs]), ((qi / kQueue) & 1u) ^ 1u, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          queue[qs] = w;
+          mbar_arrive(smem_u32(&qfull[qs]));
+          ++qi;
+        }
+        if (w < 0) break;
+        w_next = MODE == 3 ? atomicAdd(args.work_counter, 1) : w + static_cast<int>(gridDim.x);
+        Item I = item_at(args, w, nwork1);
+        if constexpr (MODE != 3) I.g = MODE - 1;
         const GemmPhase& P = args.p[I.g];
         const GemmMaps& M = I.g ? maps2 : maps1;
-        const int na = I.g ? 1 : 2;
+        const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : P.na;  // single-GEMM launches: fixed
         const int n = NT > 0 ? NT : I.tile.w;
-        const int a_row = I.tile.x * P.a_rows_per_e + I.mb * 128;
+        const int a_row = I.tile.x * P.a_rows_per_e + I.mb * P.row_step;
         const uint32_t tx = na * 16384u + static_cast<uint32_t>(n) * 128u;
         const CUtensorMap* tmb = &M.b[tok_map_index(n)];  // one box of n token rows
-        if (I.g == 1 && args.fused) {
+        if (MODE == 3 && I.g == 1) {
           // this tile's activations are written by GEMM1 items of other CTAs
           if (!wait_counter(args.dep + I.t, args.p[0].mblocks, limit, abort_flag)) {
             ok = false;
@@ -231,10 +306,27 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, tc = 0, gc = 0;
-      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
-        const Item I = item_at(args, w, nwork1);
-        const int na = I.g ? 1 : 2;
+      uint32_t it = 0, tc = 0, gc = 0, qi = 0;
+      int w_static = static_cast<int>(blockIdx.x);
+      while (ok) {
+        int w;
+        if constexpr (MODE == 3) {
+          const int qs = static_cast<int>(qi % kQueue);
+          if (!mbar_wait(smem_u32(&qfull[qs]), (qi / kQueue) & 1u, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          w = queue[qs];
+          mbar_arrive(smem_u32(&qempty[qs]));
+          ++qi;
+        } else {
+          w = w_static < nwork ? w_static : -1;
+          w_static += gridDim.x;
+        }
+        if (w < 0) break;
+        Item I = item_at(args, w, nwork1);
+        if constexpr (MODE != 3) I.g = MODE - 1;
+        const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : args.p[I.g].na;
         const int kbs = args.p[I.g].kblocks;
         const int n = NT > 0 ? NT : I.tile.w;
         const uint32_t idesc = idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(n));
@@ -265,13 +357,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           if (FP8) dbase = (buf * GS + static_cast<uint32_t>(kb % GS)) * slot_cols;
           const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * stage_bytes);
-          for (int a = 0; a < na; ++a) {
+          // descriptors built once per stage; each 32-byte K step adds 2 to
+          // the encoded start address (addresses stay below 256 KB)
+          const uint64_t bd0 = sdesc_sw128(sa + NAM * 16384);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = sdesc_sw128(sa + a * 16384 + ks * 32);
-              const uint64_t bd = sdesc_sw128(sa + NAM * 16384 + ks * 32);
-              const uint32_t accumulate = FP8 ? (ks != 0) : ((kb | ks) != 0);
-              mma_issue<KIND>(tmem_base + dbase + a * NM, ad, bd, idesc, accumulate);
+          for (int a = 0; a < 2; ++a) {
+            if (a < na) {
+              const uint64_t ad0 = sdesc_sw128(sa + a * 16384);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint32_t accumulate = FP8 ? (ks != 0) : ((kb | ks) != 0);
+                mma_issue<KIND>(tmem_base + dbase + a * NM, ad0 + 2u * ks, bd0 + 2u * ks, idesc,
+                                accumulate);
+              }
             }
           }
           mma_commit(smem_u32(&empty[s]));  // frees the stage once read
@@ -302,22 +400,48 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int part = ew >> 2;  // which half of the token columns
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
-    uint32_t tc = 0, gc = 0, eb = 0;
+    uint32_t tc = 0, gc = 0, eb = 0, qi = 0;
 
+    auto warp_arrive = [&](uint64_t* bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(bar));
+    };
     auto ep_barrier = [&]() -> bool {
-      mbar_arrive(smem_u32(epib));
+      warp_arrive(epib);
       const bool got = mbar_wait(smem_u32(epib), eb & 1u, limit, abort_flag);
       ++eb;
       return __all_sync(0xffffffffu, got);
     };
 
-    for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
-      const Item I = item_at(args, w, nwork1);
+    int w_static = static_cast<int>(blockIdx.x);
+    while (ok) {
+      int w;
+      if constexpr (MODE == 3) {
+        const int qs = static_cast<int>(qi % kQueue);
+        const bool gotq = mbar_wait(smem_u32(&qfull[qs]), (qi / kQueue) & 1u, limit, abort_flag);
+        if (!__all_sync(0xffffffffu, gotq)) {
+          ok = false;
+          break;
+        }
+        w = queue[qs];
+        warp_arrive(&qempty[qs]);
+        ++qi;
+      } else {
+        w = w_static < nwork ? w_static : -1;
+        w_static += gridDim.x;
+      }
+      if (w < 0) break;
+      Item I = item_at(args, w, nwork1);
+      if constexpr (MODE != 3) I.g = MODE - 1;
       const GemmPhase& P = args.p[I.g];
-      const int na = I.g ? 1 : 2;
+      const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : P.na;  // single-GEMM launches: fixed
       const int row0 = I.tile.y, nrows = I.tile.z;
-      const int row = I.mb * 128 + r_in_tile;  // weight row = output feature
+      // output row of accumulator a: GEMM1 gate and up share a feature row;
+      // GEMM2's second weight tile covers the next 128 output rows
+      const int row = I.mb * P.row_step + r_in_tile;
+      const int row_b = I.g ? row + 128 : row;
       const bool row_ok = row < P.m_valid;
+      const bool row_b_ok = row_b < P.m_valid;
 
       if constexpr (!FP8) {
         const int n = I.tile.w;
@@ -344,45 +468,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t dcol = sl * slot_cols;
-        for (int c0 = 0; c0 < hc; c0 += 8) {
-          const int cc = c_begin + c0;
-          if (I.g == 0) {
-            float gv[8], uv[8];
-            tmem_ld8(lane_addr + dcol + cc, gv);
-            tmem_ld8(lane_addr + dcol + NM + cc, uv);
-            tmem_wait_ld(gv, uv);
-            if (row_ok) {
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                const int j = cc + jj;
-                if (j < nrows)
-                  store_val<KIND>(args.act, static_cast<size_t>(row0 + j) * args.I + row,
-                                  silu_f(gv[jj]) * uv[jj]);
-              }
-            }
+        for (int c0 = 0; c0 < hc;) {  // 32-column chunks while they fit, then 8
+          if (hc - c0 >= 32) {
+            epi_chunk<KIND, 32>(args, I.g, na, lane_addr + dcol, NM, c_begin + c0, row0, nrows, row,
+                                row_ok, row_b, row_b_ok, cw);
+            c0 += 32;
           } else {
-            float yv[8];
-            tmem_ld8(lane_addr + dcol + cc, yv);
-            tmem_wait_ld(yv);
-            if (row_ok) {
-#pragma unroll
-              for (int jj = 0; jj < 8; ++jj) {
-                const int j = cc + jj;
-                if (j < nrows)
-                  store_val<KIND>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
-                                  cw[j] * yv[jj]);
-              }
-            }
+            epi_chunk<KIND, 8>(args, I.g, na, lane_addr + dcol, NM, c_begin + c0, row0, nrows, row,
+                               row_ok, row_b, row_b_ok, cw);
+            c0 += 8;
           }
         }
         tc_fence_before();
-        mbar_arrive(smem_u32(&acce[sl]));
+        warp_arrive(&acce[sl]);
         ++tc;
       } else {
         // -------- FP8: per-column scale products cs[a][kb][j] = s_w[a][kb] * s_x[j][kb]
         const int kbs = P.kblocks;
         const int c_begin = part * CPT;
-        if (I.g == 1 && args.fused) {
+        if (MODE == 3 && I.g == 1) {
           // the activation scales of this tile come from GEMM1 items of
           // other CTAs in this launch: acquire them (already released)
           const bool got = wait_counter(args.dep + I.t, args.p[0].mblocks, limit, abort_flag);
@@ -395,22 +499,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        const float* sw =
-            P.w_scale + (static_cast<size_t>(I.tile.x) * P.w_scale_rows_per_e + I.mb) * kbs;
+        const float* sw = P.w_scale + (static_cast<size_t>(I.tile.x) * P.w_scale_rows_per_e +
+                                       I.mb * (P.row_step / 128)) * kbs;
         for (int i = ew * 32 + lane; i < na * kbs * NT; i += EPI_THREADS) {
           const int a = i / (kbs * NT);
           const int kb = (i / NT) % kbs;
           const int j = i % NT;
-          const float swv = __ldg(sw + static_cast<size_t>(a) * (args.I / 128) * kbs + kb);
-          // L2-coherent load: GEMM2's scales may be written in this launch
-          cs[i] = (j < nrows) ? swv * __ldcg(P.b_scale + static_cast<size_t>(row0 + j) * kbs + kb)
-                              : 0.0f;
+          const float swv = __ldg(sw + static_cast<size_t>(a) * (P.a_up_off / 128) * kbs + kb);
+          const float* bs = P.b_scale + static_cast<size_t>(row0 + j) * kbs + kb;
+          // fused: GEMM2's scales are written in this launch, so read them
+          // through L2 (coherent) rather than the read-only path
+          cs[i] = (j < nrows) ? swv * (MODE == 3 ? __ldcg(bs) : __ldg(bs)) : 0.0f;
         }
+        if (I.g == 1)  // GEMM2: the routing weight of each token column
+          for (int j = ew * 32 + lane; j < NT; j += EPI_THREADS)
+            red[j] = (j < nrows) ? __ldg(args.topw + __ldg(args.src + row0 + j)) : 0.0f;
         if (!ep_barrier()) {
           ok = false;
           break;
         }
-        float acc0[CPT], acc1[CPT];  // acc1 (up) is only used by GEMM1 items
+        float acc0[CPT], acc1[CPT];  // acc1: up (GEMM1) or the second 128 rows (GEMM2)
 #pragma unroll
         for (int c = 0; c < CPT; ++c) {
           acc0[c] = 0.0f;
@@ -455,7 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_fence_before();
-          mbar_arrive(smem_u32(&acce[buf]));
+          warp_arrive(&acce[buf]);
         }
         if (!ok) break;
 
@@ -495,16 +603,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < CPT; ++c) {
             const int j = c_begin + c;
-            if (j < nrows && row_ok) {
-              const float wt = __ldg(args.topw + __ldg(args.src + row0 + j));
-              store_val<KIND_BF16>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
-                                   wt * acc0[c]);
+            if (j < nrows) {
+              const float wt = red[j];
+              if (row_ok)
+                store_val<KIND_BF16>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row,
+                                     wt * acc0[c]);
+              if (na == 2 && row_b_ok)
+                store_val<KIND_BF16>(args.ybuf, static_cast<size_t>(row0 + j) * args.H + row_b,
+                                     wt * acc1[c]);
             }
           }
         }
       }
 
-      if (I.g == 0 && args.fused) {
+      if (MODE == 3 && I.g == 0) {
         // publish this GEMM1 item: all epilogue threads' activation stores
         // become visible (to generic and TMA readers) before the count moves
         fence_proxy_async_global();
@@ -528,10 +640,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem_base, args.tmem_cols);
 }
 
-template <int KIND, int NT>
-static cudaError_t launch_one(const GemmArgs& args, const GemmMaps* maps, int grid, int smem,
-                              cudaStream_t stream) {
-  auto kern = moe_gemm_kernel<KIND, NT>;
+template <int KIND, int NT, int MODE>
+static cudaError_t launch_mode(const GemmArgs& args, const GemmMaps* maps, int grid, int smem,
+                               cudaStream_t stream) {
+  auto kern = moe_gemm_kernel<KIND, NT, MODE>;
   static int configured = 0;  // max dynamic smem is a per-function attribute
   if (configured < smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -540,6 +652,14 @@ static cudaError_t launch_one(const GemmArgs& args, const GemmMaps* maps, int gr
   }
   kern<<<grid, kThreads, smem, stream>>>(maps[0], maps[1], args);
   return cudaGetLastError();
+}
+
+template <int KIND, int NT>
+static cudaError_t launch_one(const GemmArgs& args, const GemmMaps* maps, int grid, int smem,
+                              cudaStream_t stream) {
+  if (args.run1 && args.run2) return launch_mode<KIND, NT, 3>(args, maps, grid, smem, stream);
+  if (args.run1) return launch_mode<KIND, NT, 1>(args, maps, grid, smem, stream);
+  return launch_mode<KIND, NT, 2>(args, maps, grid, smem, stream);
 }
 
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& args, const GemmMaps* maps, int grid,

@@ -28,10 +28,12 @@ __host__ __device__ inline int tok_map_index(int n) {
 struct GemmPhase {
   const int4* tiles;        // [max_tiles] {expert, first permuted row, rows, tile n}
   const int* ntiles;        // device count of valid tiles
-  int mblocks;              // 128-row weight blocks per expert (G1: ceil(I/128))
+  int na;                   // 128-row weight tiles per work item (1 or 2)
+  int row_step;             // weight rows per item index step (G1: 128; G2: 128 * na)
+  int mblocks;              // items per token tile (G1: ceil(I/128), G2: ceil(H/row_step))
   int kblocks;              // K / (128 bytes / element size)
   int a_rows_per_e;         // rows of one expert in the A view (G1: 2I, G2: H)
-  int a_up_off;             // G1: I (first up row); G2: 0
+  int a_up_off;             // rows from the first to the second weight tile (G1: I, G2: 128)
   int m_valid;              // G1: I, G2: H -- weight rows at or beyond are masked
   const float* w_scale;     // FP8 weight block scales (s13 / s2)
   int w_scale_rows_per_e;   // G1: 2I/128, G2: H/128
@@ -43,12 +45,14 @@ struct GemmPhase {
 // permuted token rows of that expert; each tile carries its own n).  A
 // launch runs GEMM1 items, GEMM2 items, or both: fused, GEMM2 items follow
 // GEMM1's in one work list and each waits until all GEMM1 items of its
-// token tile have finished (dep counters).
+// token tile have finished (dep counters); there CTAs take items in list
+// order through a global counter, so faster CTAs take more items.
 struct GemmArgs {
   GemmPhase p[2];      // [0] gate+up GEMM, [1] down GEMM
   int run1, run2;      // which GEMMs this launch runs
   int fused;           // both, sharing tile list p[0]; GEMM2 waits on dep
   int* dep;            // [max_tiles] finished GEMM1 items per tile (fused)
+  int* work_counter;   // next work item of this launch (zeroed before the launch)
   int n_max;           // largest tile n (stage and TMEM slot size)
   int na_max;          // weight tiles per stage: 2 if GEMM1 runs, else 1
   int R;               // permuted rows (T*k)
@@ -76,7 +80,7 @@ inline int gemm_stage_bytes(int na, int n_max) { return na * 16384 + n_max * 128
 // of the longer K and the per-column amax exchange; otherwise GEMM2's
 // per-column weights)
 inline int gemm_extra_smem(int n_max, int kblocks_max, bool fp8) {
-  return 1024 /* align slack */ + 512 /* barriers, flags */ +
+  return 1024 /* align slack */ + 1024 /* barriers, work queue, flags */ +
          (fp8 ? 2 * n_max * kblocks_max * 4 + 4 * n_max * 4 : n_max * 4);
 }
 

@@ -239,7 +239,8 @@ __global__ void __launch_bounds__(1024)
                 int4* __restrict__ tiles2, int* __restrict__ ntiles2, int* __restrict__ dep,
                 unsigned* __restrict__ err) {
   __shared__ int warp_sums[32];
-  for (int i = threadIdx.x; i < max_tiles; i += blockDim.x) dep[i] = 0;  // fused GEMM counters
+  // fused-GEMM tile counters and the two work counters that follow them
+  for (int i = threadIdx.x; i < max_tiles + 2; i += blockDim.x) dep[i] = 0;
   __shared__ int tot_rows, tot_tiles1, tot_tiles2;
   const int e = threadIdx.x;
   int cnt = 0;
@@ -628,11 +629,20 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const int kb1 = H / (128 / esize), kb2 = I / (128 / esize);
   const int kbmax = kb1 > kb2 ? kb1 : kb2;
   GemmArgs g{};
-  g.p[0] = GemmPhase{tiles, ntiles, p->g1_mblocks, kb1, 2 * I, I, I, s13, fp8 ? 2 * I / 128 : 0,
-                     xs};
-  const bool fused = NM1 == NM2;  // one tile list: GEMM2 items follow GEMM1's in one launch
-  g.p[1] = GemmPhase{fused ? tiles : tiles2, fused ? ntiles : ntiles2, p->g2_mblocks, kb2, H, 0,
-                     H, s2, fp8 ? H / 128 : 0, as};
+  g.p[0] = GemmPhase{tiles, ntiles, 2, 128, p->g1_mblocks, kb1, 2 * I, I, I, s13,
+                     fp8 ? 2 * I / 128 : 0, xs};
+  // one launch for both GEMMs when they share a tile list and experts hold
+  // few rows (est <= 32): GEMM2 work then fills the tail of GEMM1's.  With
+  // more rows per expert GEMM1's items are many and short relative to the
+  // whole, and two launches with their own stage layouts run faster.
+  const bool fused = NM1 == NM2 && p->est <= 32;
+  // fused GEMM2 items take two 128-row weight tiles (256 output rows), so
+  // that they stream as many weight bytes per stage as GEMM1 items
+  const int na2 = (fused && H % 256 == 0) ? 2 : 1;
+  const bool one_list = NM1 == NM2;  // the scan writes list 2 only when widths differ
+  g.p[1] = GemmPhase{one_list ? tiles : tiles2, one_list ? ntiles : ntiles2, na2, 128 * na2,
+                     (H + 128 * na2 - 1) / (128 * na2), kb2, H, 128, H, s2,
+                     fp8 ? H / 128 : 0, as};
   g.dep = dep;
   g.R = static_cast<int>(R);
   g.act = act;
@@ -646,6 +656,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   g.limit_ns = kWaitLimitNs;
   const GemmMaps maps[2] = {m1, m2};
   auto launch = [&](int run1, int run2, int nm, int na) -> bool {
+    g.work_counter = dep + p->max_tiles + (run1 ? 0 : 1);  // zeroed by the scan
     g.run1 = run1;
     g.run2 = run2;
     g.fused = run1 && run2;
@@ -655,7 +666,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
     g.nslots = slots_for(na, nm, fp8);
     g.tmem_cols = tmem_cols_for(g.nslots * na * nm);
     const long long work = static_cast<long long>(p->max_tiles) *
-                           ((run1 ? p->g1_mblocks : 0) + (run2 ? p->g2_mblocks : 0));
+                           ((run1 ? g.p[0].mblocks : 0) + (run2 ? g.p[1].mblocks : 0));
     const int grid = static_cast<int>(work < sms ? work : sms);
     const int smem = g.stages * gemm_stage_bytes(na, nm) + gemm_extra_smem(nm, kbmax, fp8);
     return launch_grouped_gemm(kind, g, maps, grid, smem, st) == cudaSuccess;
@@ -762,7 +773,7 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   p.off_ntiles = take(16);
   p.off_tiles2 = take(static_cast<uint64_t>(max_tiles) * 16);
   p.off_ntiles2 = take(16);
-  p.off_dep = take(static_cast<uint64_t>(max_tiles) * 4);
+  p.off_dep = take(static_cast<uint64_t>(max_tiles + 2) * 4);
   p.off_xq = take(static_cast<uint64_t>(R) * H * ex);
   p.off_xs = take(dtype == MOE_DTYPE_FP8_BLOCK128 ? static_cast<uint64_t>(R) * (H / 128) * 4 : 0);
   p.off_act = take(static_cast<uint64_t>(R) * I * ex);
