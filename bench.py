@@ -54,6 +54,28 @@ def parse():
     return ap.parse_args()
 
 
+def ncu_traffic(workload):
+    """DRAM bytes (read + write) per launch of the dominant GEMM kernel from
+    the committed ncu summary, if it was taken from the current kernel
+    sources; else None."""
+    import glob
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "serving_moe_route_gb300", "csrc")
+    for fn in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(fn, "rb") as f:
+            h.update(f.read())
+    e = d.get("entries", {}).get(workload)
+    if e is None or d.get("source_sha256") != h.hexdigest():
+        return None
+    return int(e["dram_read_bytes"] + e["dram_write_bytes"])
+
+
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -459,7 +481,11 @@ def run_ours(args):
 
     acc = algorithmic(wl, r.counts())
     gname, groof = gemm_roofline(wl, st, acc, pk)
-    launches_per_step = 5 if wl.dtype == W.F32 else 6
+    groof["traffic"] = ncu_traffic(wl.name)
+    groof["traffic_source"] = ("profiles/ncu_traffic.json (ncu --set full, same kernel sources)"
+                               if groof["traffic"] is not None else None)
+    fused = statistics.mean(st["gemm2"]) < 0.02 * statistics.mean(st["gemm1"])
+    launches_per_step = 5 if fused else 6
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
