@@ -185,8 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* epib = done + 1;   // epilogue-internal barrier
   uint64_t* qfull = epib + 1;  // [kQueue] work-queue entry written
   uint64_t* qempty = qfull + kQueue;  // [kQueue] entry read by the MMA thread and the epilogue
-  int* queue = reinterpret_cast<int*>(qempty + kQueue);  // [kQueue] item indices, -1 = end
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(queue + kQueue);
+  // [kQueue] work items (index w, -1 = end, and the item's tile) handed over
+  Item* queue = reinterpret_cast<Item*>(
+      (reinterpret_cast<uintptr_t>(qempty + kQueue) + 15) & ~static_cast<uintptr_t>(15));
+  int* queue_w = reinterpret_cast<int*>(queue + kQueue);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(queue_w + kQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* cs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 1024);
   // FP8: [4][NM] per-column amax per lane quadrant (GEMM1), column weights (GEMM2)
@@ -247,8 +250,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // taken one item ahead so the atomic's latency overlaps the loads.
       // Single-GEMM launches walk the list with a grid stride.
       int w_next = MODE == 3 ? atomicAdd(args.work_counter, 1) : static_cast<int>(blockIdx.x);
+      Item nxt{};  // the next item's tile, loaded one item ahead
+      if (w_next < nwork) nxt = item_at(args, w_next, nwork1);
       while (ok) {
         const int w = w_next < nwork ? w_next : -1;
+        Item I = nxt;
         if constexpr (MODE == 3) {
           // hand the item to the MMA thread and the epilogue
           const int qs = static_cast<int>(qi % kQueue);
@@ -256,13 +262,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          queue[qs] = w;
+          queue[qs] = I;
+          queue_w[qs] = w;
           mbar_arrive(smem_u32(&qfull[qs]));
           ++qi;
         }
         if (w < 0) break;
         w_next = MODE == 3 ? atomicAdd(args.work_counter, 1) : w + static_cast<int>(gridDim.x);
-        Item I = item_at(args, w, nwork1);
+        if (w_next < nwork) nxt = item_at(args, w_next, nwork1);
         if constexpr (MODE != 3) I.g = MODE - 1;
         const GemmPhase& P = args.p[I.g];
         const GemmMaps& M = I.g ? maps2 : maps1;
@@ -308,24 +315,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0, tc = 0, gc = 0, qi = 0;
       int w_static = static_cast<int>(blockIdx.x);
+      Item nxt{};
+      if (MODE != 3 && w_static < nwork) nxt = item_at(args, w_static, nwork1);
       while (ok) {
         int w;
+        Item I;
         if constexpr (MODE == 3) {
           const int qs = static_cast<int>(qi % kQueue);
           if (!mbar_wait(smem_u32(&qfull[qs]), (qi / kQueue) & 1u, limit, abort_flag)) {
             ok = false;
             break;
           }
-          w = queue[qs];
+          w = queue_w[qs];
+          I = queue[qs];
           mbar_arrive(smem_u32(&qempty[qs]));
           ++qi;
         } else {
           w = w_static < nwork ? w_static : -1;
+          I = nxt;
           w_static += gridDim.x;
+          if (w >= 0 && w_static < nwork) nxt = item_at(args, w_static, nwork1);
+          I.g = MODE - 1;
         }
         if (w < 0) break;
-        Item I = item_at(args, w, nwork1);
-        if constexpr (MODE != 3) I.g = MODE - 1;
         const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : args.p[I.g].na;
         const int kbs = args.p[I.g].kblocks;
         const int n = NT > 0 ? NT : I.tile.w;
@@ -414,8 +426,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     int w_static = static_cast<int>(blockIdx.x);
+    Item nxt{};
+    if (MODE != 3 && w_static < nwork) nxt = item_at(args, w_static, nwork1);
     while (ok) {
       int w;
+      Item I;
       if constexpr (MODE == 3) {
         const int qs = static_cast<int>(qi % kQueue);
         const bool gotq = mbar_wait(smem_u32(&qfull[qs]), (qi / kQueue) & 1u, limit, abort_flag);
@@ -423,16 +438,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        w = queue[qs];
+        w = queue_w[qs];
+        I = queue[qs];
         warp_arrive(&qempty[qs]);
         ++qi;
       } else {
         w = w_static < nwork ? w_static : -1;
+        I = nxt;
         w_static += gridDim.x;
+        if (w >= 0 && w_static < nwork) nxt = item_at(args, w_static, nwork1);
+        I.g = MODE - 1;
       }
       if (w < 0) break;
-      Item I = item_at(args, w, nwork1);
-      if constexpr (MODE != 3) I.g = MODE - 1;
       const GemmPhase& P = args.p[I.g];
       const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : P.na;  // single-GEMM launches: fixed
       const int row0 = I.tile.y, nrows = I.tile.z;
