@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--workload", default="decode_bf16")
     ap.add_argument("--sweep", action="store_true", help="also time every workload (rank 0)")
     ap.add_argument("--sweep-samples", type=int, default=24)
+    ap.add_argument("--routing", action="store_true",
+                    help="also run the routing micro-benchmark (rank 0)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -301,6 +303,21 @@ class Runner:
         return self.layer.intermediates(self.wl.T)["counts"].cpu().tolist()
 
 
+def job_throughput(local_seconds, units_per_rank, device=None):
+    """Whole-job throughput of independent replicas: every rank processed
+    units_per_rank units; the job's time is the max over ranks of their timed
+    regions (all_reduce MAX).  Returns (units/s over all ranks, job seconds)."""
+    import torch
+    import torch.distributed as dist
+    world = dist.get_world_size() if dist.is_available() and dist.is_initialized() else 1
+    t = float(local_seconds)
+    if world > 1:
+        x = torch.tensor([t], dtype=torch.float64, device=device)
+        dist.all_reduce(x, op=dist.ReduceOp.MAX)
+        t = float(x.item())
+    return world * units_per_rank / t, t
+
+
 def pct(v, q):
     s = sorted(v)
     return s[min(len(s) - 1, max(0, int(round(q * (len(s) - 1)))))]
@@ -386,6 +403,43 @@ def cpu_baseline(wl, inp, seconds):
                       f"for those tokens), {dt:.2f} s, OpenMP over tokens"}
 
 
+def routing_bench(dev, calls=500):
+    """The routing micro-benchmark of PR #39593 ("Test Plan", item 3): 128
+    tokens x 128 experts, top-8, bf16 logits with 10% all-NaN rows.  moe_route_topk
+    (NaN sanitised in registers) against the same call behind a separate
+    nan_to_num launch; per-call CUDA-event times, p20/p50/p80 in µs."""
+    import torch
+
+    from serving_moe_route_gb300 import route_topk
+    from serving_moe_route_gb300 import workloads as W
+    wl = W.workloads()["decode_bf16"]
+    lg = W.make_logits(wl).to(dev)
+    out = {}
+    for scoring, sname in ((W.SOFTMAX, "topk_softmax"), (W.SIGMOID, "topk_sigmoid")):
+        for variant in ("fused", "separate_nan_to_num"):
+            def call():
+                x = lg
+                if variant != "fused":
+                    x = torch.nan_to_num(lg, nan=float("-inf"))
+                return route_topk(x, wl.k, scoring=scoring, renorm=True)
+            for _ in range(20):
+                call()
+            torch.cuda.synchronize(dev)
+            pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                     for _ in range(calls)]
+            for a, b in pairs:
+                a.record()
+                call()
+                b.record()
+            torch.cuda.synchronize(dev)
+            us = [a.elapsed_time(b) * 1e3 for a, b in pairs]
+            out[f"{sname}_{variant}"] = {"p20": round(pct(us, 0.2), 2),
+                                         "p50": round(pct(us, 0.5), 2),
+                                         "p80": round(pct(us, 0.8), 2)}
+    out["config"] = "T=128, E=128, top-8, bf16 logits, 13 all-NaN rows; eager calls"
+    return out
+
+
 def sweep(dev, samples, pk):
     """Every workload: median/p20/p80 us per call, tokens/s, roofline."""
     import torch
@@ -464,20 +518,12 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     st = r.run_stages(min(steps, 100))
 
-    total_s = sum(step_ms) * 1e-3
-    if world > 1:
-        t = torch.tensor([total_s], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_s = float(t.item())
+    value, total_s = job_throughput(sum(step_ms) * 1e-3, steps * wl.T, dev)
     ms_per_step = total_s * 1e3 / steps
-    value = world * steps * wl.T / total_s
 
-    e2e_ms, h2d, d2h = r.run_e2e(max(10, min(steps, 200)), 3)
-    e2e_val = wl.T / (statistics.mean(e2e_ms) * 1e-3)
-    if world > 1:
-        t = torch.tensor([statistics.mean(e2e_ms)], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_val = world * wl.T / (float(t.item()) * 1e-3)
+    e2e_steps = max(10, min(steps, 200))
+    e2e_ms, h2d, d2h = r.run_e2e(e2e_steps, 3)
+    e2e_val, _ = job_throughput(sum(e2e_ms) * 1e-3, e2e_steps * wl.T, dev)
 
     acc = algorithmic(wl, r.counts())
     gname, groof = gemm_roofline(wl, st, acc, pk)
@@ -514,6 +560,8 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
+    if rank == 0 and (args.sweep or args.routing):
+        line["routing_microbench"] = routing_bench(dev)
     if rank == 0 and args.sweep:
         del r
         line["sweep"] = sweep(dev, args.sweep_samples, pk)
