@@ -36,6 +36,7 @@ HBM_NORTH_STAR_GBS = 8000.0
 FLUSH_BYTES = 256 << 20
 SWEEP = ["decode_bf16", "sparse_uniform_bf16", "sparse_concentrated_bf16",
          "sparse_uniform_bf16_old_est", "sparse_concentrated_bf16_old_est",
+         "sparse_uniform_bf16_ep8", "sparse_uniform_bf16_ep8_old_est",
          "fp8_T1", "fp8_T2", "fp8_T4", "fp8_T16", "fp8_T64", "fp8_T128", "fp8_T256", "fp8_T1024",
          "fp8_T4096", "skewed_prefill_bf16", "skewed_prefill_sigmoid_bf16", "tiny_f32"]
 
@@ -187,7 +188,7 @@ class Runner:
         s2 = inp["s2"].to(dev) if inp["s2"] is not None else None
         self.layer = MoELayer(inp["w13"].to(dev), inp["w2"].to(dev), k=wl.k, dtype=wl.dtype,
                               scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2,
-                              force_est=wl.force_est)
+                              force_est=wl.force_est, ep_size=wl.ep_size, ep_rank=wl.ep_rank)
         self.x = inp["x"].to(dev)
         self.lg = inp["logits"].to(dev)
         self.out = torch.empty(wl.T, wl.H, dtype=self.x.dtype, device=dev)
@@ -386,7 +387,7 @@ def cpu_baseline(wl, inp, seconds):
                 renorm=wl.renorm, x=W.storage_numpy(inp["x"]),
                 logits=W.storage_numpy(inp["logits"]), w13=W.storage_numpy(inp["w13"]),
                 w2=W.storage_numpy(inp["w2"]), s13=W.storage_numpy(inp["s13"]),
-                s2=W.storage_numpy(inp["s2"]))
+                s2=W.storage_numpy(inp["s2"]), ep_size=wl.ep_size, ep_rank=wl.ep_rank)
     n = min(wl.T, max(1, cores))
     t0 = time.perf_counter()
     oracle.moe_forward(**args, tokens=np.arange(n, dtype=np.int32))
@@ -422,21 +423,34 @@ def routing_bench(dev, calls=500):
                 if variant != "fused":
                     x = torch.nan_to_num(lg, nan=float("-inf"))
                 return route_topk(x, wl.k, scoring=scoring, renorm=True)
-            for _ in range(20):
+            side = torch.cuda.Stream(dev)
+            side.wait_stream(torch.cuda.current_stream(dev))
+            with torch.cuda.stream(side):
+                for _ in range(3):
+                    call()
+            torch.cuda.current_stream(dev).wait_stream(side)
+            torch.cuda.synchronize(dev)
+            # one graph per variant, replayed: device time per call without
+            # the host's per-call launch cost
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
                 call()
+            for _ in range(20):
+                g.replay()
             torch.cuda.synchronize(dev)
             pairs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                      for _ in range(calls)]
             for a, b in pairs:
                 a.record()
-                call()
+                g.replay()
                 b.record()
             torch.cuda.synchronize(dev)
             us = [a.elapsed_time(b) * 1e3 for a, b in pairs]
             out[f"{sname}_{variant}"] = {"p20": round(pct(us, 0.2), 2),
                                          "p50": round(pct(us, 0.5), 2),
                                          "p80": round(pct(us, 0.8), 2)}
-    out["config"] = "T=128, E=128, top-8, bf16 logits, 13 all-NaN rows; eager calls"
+    out["config"] = ("T=128, E=128, top-8, bf16 logits, 13 all-NaN rows; CUDA-graph replays, "
+                     "events around each replay")
     return out
 
 
@@ -450,8 +464,8 @@ def sweep(dev, samples, pk):
     rows = []
     for name in SWEEP:
         wl = wls[name]
-        key = (wl.H, wl.I, wl.E, wl.dtype, wl.seed)
-        if key != wkey:  # weights depend on (H, I, E, dtype, seed) only
+        key = (wl.H, wl.I, wl.E, wl.dtype, wl.seed, wl.ep_size, wl.ep_rank)
+        if key != wkey:  # weights depend on (H, I, E, dtype, seed, ep slice) only
             weights = None
             torch.cuda.empty_cache()
             wkey, weights = key, W.make_weights(wl)
@@ -589,7 +603,8 @@ def run_reference(args):
     fa = dict(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, dtype=wl.dtype, scoring=wl.scoring,
               renorm=wl.renorm, x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
               w13=W.storage_numpy(inp["w13"]), w2=W.storage_numpy(inp["w2"]),
-              s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]))
+              s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]),
+              ep_size=wl.ep_size, ep_rank=wl.ep_rank)
     n = min(wl.T, max(1, cores))  # tokens per step: one per host core
     toks = np.arange(n, dtype=np.int32)
     for _ in range(max(0, args.warmup)):

@@ -88,8 +88,8 @@ extern "C" {
  * can read the intermediates:
  *   ids     int32 [T, k]    chosen expert per pick (-1 = skipped, see with_ids)
  *   w       f32   [T, k]    combine weight per pick
- *   counts  int32 [E]       rows per expert
- *   offsets int32 [E + 1]   exclusive scan of counts
+ *   counts  int32 [e_local] rows per (local) expert
+ *   offsets int32 [e_local + 1] exclusive scan of counts
  *   src     int32 [T*k]     permuted row -> flat index (expert-major,
  *                           ascending flat index within an expert)
  *   pos     int32 [T*k]     flat index -> permuted row (inverse of src)
@@ -122,6 +122,9 @@ typedef struct moe_plan {
   int32_t max_tiles;  /* worst-case token tiles (independent of est) */
   int32_t g1_mblocks; /* ceil(I / 128) gate+up feature blocks */
   int32_t g2_mblocks; /* ceil(H / 128) output feature blocks */
+  int32_t ep_size;    /* expert-parallel ranks (1: all experts local) */
+  int32_t ep_rank;    /* this rank; it holds experts [ep_rank*e_local, +e_local) */
+  int32_t e_local;    /* E / ep_size: experts in w13/w2/s13/s2 of this call */
   int32_t reserved0;
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
@@ -146,6 +149,23 @@ typedef struct moe_plan {
  */
 int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm, int force_est,
              moe_plan_t* plan);
+
+/*
+ * moe_plan_ep -- moe_plan for one expert-parallel rank (H20 article,
+ * para. 2: the fused-MoE API takes the expert-parallel size and rank).  E is
+ * the number of experts over all ranks (E % ep_size == 0); this rank holds
+ * experts [ep_rank*E/ep_size, (ep_rank+1)*E/ep_size), and w13/w2/s13/s2
+ * passed with this plan hold only those e_local = E/ep_size experts.
+ * Routing ranks all E experts (logits [T, E]); picks of other ranks'
+ * experts are skipped, so out is this rank's partial sum -- the layer's
+ * output is the sum over ranks (the exchange between ranks is the caller's).
+ * The estimate divides by all E experts.  counts/offsets/tiles use local
+ * expert indices; ids keep the global ones.  moe_plan is moe_plan_ep with
+ * ep_size 1, ep_rank 0.  Errors as moe_plan, and MOE_ERR_INVALID_ARG for a
+ * bad ep_size / ep_rank.
+ */
+int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm,
+                int force_est, int ep_size, int ep_rank, moe_plan_t* plan);
 
 /*
  * moe_forward -- steps a-1 .. a-7 for one batch, asynchronously on stream.

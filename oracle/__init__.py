@@ -66,7 +66,8 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_route.restype = i
         _lib.oracle_permute.argtypes = [P, i, i, P, P, P, P]
         _lib.oracle_permute.restype = i
-        _lib.oracle_moe_forward.argtypes = [i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, i, P, P, P]
+        _lib.oracle_moe_forward.argtypes = [i, i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, i,
+                                            P, P, P]
         _lib.oracle_moe_forward.restype = i
         _lib.oracle_set_threads.argtypes = [i]
         _lib.oracle_set_threads.restype = None
@@ -141,8 +142,10 @@ def permute(ids: np.ndarray, E: int):
 
 
 def moe_forward(*, T, H, I, E, k, dtype, scoring, renorm, x, logits, w13, w2, s13=None, s2=None,
-                tokens=None):
-    """Fused MoE forward for the listed tokens (default: all).
+                tokens=None, ep_size=1, ep_rank=0):
+    """Fused MoE forward for the listed tokens (default: all).  With
+    ep_size > 1, w13/w2/s13/s2 hold rank ep_rank's E/ep_size experts and the
+    output is that rank's partial sum.
 
     Returns (out float64 [n, H], ids int32 [n, k], w float64 [n, k]).
     """
@@ -152,7 +155,7 @@ def moe_forward(*, T, H, I, E, k, dtype, scoring, renorm, x, logits, w13, w2, s1
     ids = np.empty((n, k), np.int32)
     w = np.empty((n, k), np.float64)
     rc = lib().oracle_moe_forward(
-        T, H, I, E, k, dtype, scoring, int(bool(renorm)),
+        T, H, I, E, k, dtype, scoring, int(bool(renorm)), ep_size, ep_rank,
         _ptr(x), _ptr(logits), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2),
         _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w))
     if rc != 0:

@@ -291,6 +291,11 @@ static void fake_quant_row(const float* v, int n, double* out, uint8_t* codes, f
 
 /*
  * The fused MoE layer forward for a list of tokens.
+ * Expert parallelism (H20 article, para. 2: the fused-MoE API takes the
+ * expert-parallel size and rank): with ep_size > 1 the weights hold only
+ * the E / ep_size experts of rank ep_rank (global ids ep_rank*E/ep_size ..
+ * +E/ep_size - 1); routing still ranks all E experts, and picks outside the
+ * local range contribute nothing, so out is this rank's partial sum.
  *   dtype 0: x [T,H] f32, logits [T,E] f32, w13 [E,2I,H] f32, w2 [E,H,I] f32
  *   dtype 1: x, logits, w13, w2 as bf16 bit patterns (uint16)
  *   dtype 2: x, logits bf16; w13, w2 e4m3 codes with fp32 block scales
@@ -301,10 +306,13 @@ static void fake_quant_row(const float* v, int n, double* out, uint8_t* codes, f
  * (either may be NULL).  Returns 0, or -1 on unsupported sizes.
  */
 int oracle_moe_forward(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm,
-                       const void* x, const void* logits, const void* w13, const float* s13,
-                       const void* w2, const float* s2, const int32_t* tokens, int n_tokens,
-                       double* out, int32_t* ids_out, double* w_out) {
+                       int ep_size, int ep_rank, const void* x, const void* logits,
+                       const void* w13, const float* s13, const void* w2, const float* s2,
+                       const int32_t* tokens, int n_tokens, double* out, int32_t* ids_out,
+                       double* w_out) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || E > 1024 || k < 1 || k > E) return -1;
+  if (ep_size < 1 || E % ep_size != 0 || ep_rank < 0 || ep_rank >= ep_size) return -1;
+  const int e_local = E / ep_size, e_base = ep_rank * e_local;
   if (dtype == ORACLE_DTYPE_FP8 && (H % 128 != 0 || I % 128 != 0)) return -1;
   if (!tokens) n_tokens = T;
 
@@ -363,7 +371,8 @@ int oracle_moe_forward(int T, int H, int I, int E, int k, int dtype, int scoring
 
     for (int h = 0; h < H; ++h) orow[h] = 0.0;
     for (int j = 0; j < k; ++j) {
-      int e = ids[j];
+      int e = ids[j] - e_base; /* index into this rank's weights */
+      if (e < 0 || e >= e_local) continue; /* another rank's expert */
       /* a-4, a-5: gate and up projections, SiLU(gate) * up */
       for (int c = 0; c < I; ++c) {
         double g = 0.0, u = 0.0;

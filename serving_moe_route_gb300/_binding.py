@@ -27,7 +27,7 @@ MOE_DTYPE_F32, MOE_DTYPE_BF16, MOE_DTYPE_FP8_BLOCK128 = 0, 1, 2
 MOE_LOGITS_F32, MOE_LOGITS_BF16 = 0, 1
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 
-EXPORTED = ("moe_plan", "moe_forward", "moe_forward_timed", "moe_forward_with_ids",
+EXPORTED = ("moe_plan", "moe_plan_ep", "moe_forward", "moe_forward_timed", "moe_forward_with_ids",
             "moe_forward_noalloc", "moe_route_topk", "moe_check", "moe_plan_describe",
             "moe_strerror", "moe_abi_version")
 
@@ -36,7 +36,8 @@ class MoePlan(ctypes.Structure):
     """Mirror of ``moe_plan_t``."""
     _fields_ = [(n, c_i32) for n in (
         "abi_version", "T", "H", "I", "E", "k", "dtype", "scoring", "renorm", "est", "force_est",
-        "tile_n", "route_tpc", "n_chunks", "max_tiles", "g1_mblocks", "g2_mblocks", "reserved0")]
+        "tile_n", "route_tpc", "n_chunks", "max_tiles", "g1_mblocks", "g2_mblocks", "ep_size",
+        "ep_rank", "e_local", "reserved0")]
     _fields_ += [(n, c_u64) for n in (
         "workspace_bytes", "off_err", "off_ids", "off_w", "off_chunk_counts", "off_lrank",
         "off_counts", "off_offsets", "off_chunk_base", "off_src", "off_pos", "off_tiles",
@@ -82,6 +83,8 @@ def lib() -> ctypes.CDLL:
     L.moe_strerror.restype = ctypes.c_char_p
     L.moe_plan.argtypes = [i, i, i, i, i, i, i, i, i, ctypes.POINTER(MoePlan)]
     L.moe_plan.restype = i
+    L.moe_plan_ep.argtypes = [i, i, i, i, i, i, i, i, i, i, i, ctypes.POINTER(MoePlan)]
+    L.moe_plan_ep.restype = i
     L.moe_plan_describe.argtypes = [ctypes.POINTER(MoePlan), ctypes.c_char_p, ctypes.c_size_t]
     L.moe_plan_describe.restype = i
     L.moe_forward.argtypes = [ctypes.POINTER(MoePlan), P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
@@ -121,6 +124,14 @@ def moe_plan(T, H, I, E, k, dtype, scoring=MOE_SCORING_SOFTMAX, renorm=True, for
     p = MoePlan()
     _check(lib().moe_plan(T, H, I, E, k, dtype, scoring, int(bool(renorm)), force_est,
                           ctypes.byref(p)), "moe_plan")
+    return p
+
+
+def moe_plan_ep(T, H, I, E, k, dtype, scoring=MOE_SCORING_SOFTMAX, renorm=True, force_est=0,
+                ep_size=1, ep_rank=0):
+    p = MoePlan()
+    _check(lib().moe_plan_ep(T, H, I, E, k, dtype, scoring, int(bool(renorm)), force_est,
+                             ep_size, ep_rank, ctypes.byref(p)), "moe_plan_ep")
     return p
 
 

@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kRouteThreads)
     route_kernel(const LT* __restrict__ logits, int T, int E, int k, int scoring, int renorm,
                  int tpc, int mode, const int* __restrict__ ids_in, const float* __restrict__ w_in,
                  int* __restrict__ ids, float* __restrict__ w, int* __restrict__ chunk_counts,
-                 int* __restrict__ lrank, unsigned* __restrict__ err) {
+                 int* __restrict__ lrank, unsigned* __restrict__ err, int e_base, int e_local) {
   extern __shared__ int sid[];  // [tpc * k] picks of this CTA's tokens
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * tpc;
@@ -152,7 +152,11 @@ __global__ void __launch_bounds__(kRouteThreads)
     if (lane < k) {
       ids[static_cast<size_t>(t) * k + lane] = my_id;
       w[static_cast<size_t>(t) * k + lane] = my_w;
-      if (mode != 0) sid[tl * k + lane] = my_id;
+      // histogram and permutation see this rank's experts only (local index);
+      // picks of other expert-parallel ranks' experts are skipped (-1)
+      if (mode != 0)
+        sid[tl * k + lane] =
+            (my_id >= e_base && my_id < e_base + e_local) ? my_id - e_base : -1;
     }
   }
   if (mode == 0) return;
@@ -166,10 +170,10 @@ __global__ void __launch_bounds__(kRouteThreads)
     for (int g = 0; g < f; ++g) r += (sid[g] == e);
     lrank[static_cast<size_t>(t0) * k + f] = (e >= 0) ? r : -1;
   }
-  for (int e = threadIdx.x; e < E; e += kRouteThreads) {
+  for (int e = threadIdx.x; e < e_local; e += kRouteThreads) {
     int c = 0;
     for (int f = 0; f < n; ++f) c += (sid[f] == e);
-    chunk_counts[static_cast<size_t>(blockIdx.x) * E + e] = c;
+    chunk_counts[static_cast<size_t>(blockIdx.x) * e_local + e] = c;
   }
 }
 
@@ -272,9 +276,9 @@ template <int QT>
 __global__ void __launch_bounds__(256)
     gather_kernel(const void* __restrict__ x, const int* __restrict__ ids,
                   const int* __restrict__ lrank, const int* __restrict__ chunk_base,
-                  const int* __restrict__ offsets, int T, int H, int E, int k, int tpc,
-                  int* __restrict__ src, int* __restrict__ pos, void* __restrict__ xq,
-                  float* __restrict__ xs) {
+                  const int* __restrict__ offsets, int T, int H, int k, int tpc, int e_base,
+                  int e_local, int* __restrict__ src, int* __restrict__ pos,
+                  void* __restrict__ xq, float* __restrict__ xs) {
   const int lane = threadIdx.x & 31;
   const int chunks = (H + 255) / 256;
   const long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -285,9 +289,10 @@ __global__ void __launch_bounds__(256)
   int my_slot = -1;
   if (lane < k) {
     const size_t f = static_cast<size_t>(t) * k + lane;
-    const int e = ids[f];
-    if (e >= 0)
-      my_slot = offsets[e] + chunk_base[static_cast<size_t>(t / tpc) * E + e] + lrank[f];
+    const int eg = ids[f];  // global id; -1 = skipped pick
+    const int e = eg - e_base;
+    if (eg >= 0 && e >= 0 && e < e_local)
+      my_slot = offsets[e] + chunk_base[static_cast<size_t>(t / tpc) * e_local + e] + lrank[f];
     if (c == 0) {
       pos[f] = my_slot;
       if (my_slot >= 0) src[my_slot] = static_cast<int>(f);
@@ -433,12 +438,12 @@ template <typename LT>
 static void launch_route_t(int vpt, dim3 grid, size_t smem, cudaStream_t st, const LT* logits,
                            int T, int E, int k, int scoring, int renorm, int tpc, int mode,
                            const int* ids_in, const float* w_in, int* ids, float* w, int* cc,
-                           int* lr, unsigned* err) {
+                           int* lr, unsigned* err, int e_base, int e_local) {
 #define MOE_ROUTE_CASE(V)                                                                      \
   case V:                                                                                      \
     route_kernel<V, LT><<<grid, kRouteThreads, smem, st>>>(logits, T, E, k, scoring, renorm, \
                                                            tpc, mode, ids_in, w_in, ids, w,  \
-                                                           cc, lr, err);                     \
+                                                           cc, lr, err, e_base, e_local);    \
     break;
   switch (vpt) {
     MOE_ROUTE_CASE(1)
@@ -517,7 +522,8 @@ static uint32_t tmem_cols_for(int need) {
 
 static int plan_ok(const moe_plan_t* p) {
   return p && p->abi_version == MOE_ABI_VERSION && p->T >= 0 && p->E >= 1 && p->k >= 1 &&
-         p->tile_n >= 16;
+         p->tile_n >= 16 && p->ep_size >= 1 && p->e_local >= 1 &&
+         p->e_local * p->ep_size == p->E && p->ep_rank >= 0 && p->ep_rank < p->ep_size;
 }
 
 // the common forward; ids_in/w_in non-null selects caller-supplied routing
@@ -560,6 +566,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   void* ybuf = at(p->off_y);
 
   const int T = p->T, H = p->H, I = p->I, E = p->E, k = p->k;
+  const int EL = p->e_local, e_base = p->ep_rank * p->e_local;  // this rank's experts
   const long long R = static_cast<long long>(T) * k;
   auto mark = [&](int i) {
     if (events) cudaEventRecord(static_cast<cudaEvent_t>(events[i]), st);
@@ -573,12 +580,13 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   if (p->dtype == MOE_DTYPE_F32)
     launch_route_t<float>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
                           static_cast<const float*>(logits), T, E, k, p->scoring, p->renorm,
-                          p->route_tpc, mode, ids_in, w_in, ids, topw, chunk_counts, lrank, err);
+                          p->route_tpc, mode, ids_in, w_in, ids, topw, chunk_counts, lrank, err,
+                          e_base, EL);
   else
     launch_route_t<__nv_bfloat16>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
                                   static_cast<const __nv_bfloat16*>(logits), T, E, k, p->scoring,
                                   p->renorm, p->route_tpc, mode, ids_in, w_in, ids, topw,
-                                  chunk_counts, lrank, err);
+                                  chunk_counts, lrank, err, e_base, EL);
   mark(1);
   // a-2 / a-3 scan and tile list
   const int per_expert = fp8 ? 0 : 1;
@@ -588,7 +596,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   // prefill-sized plans (est > 64).
   const int NM1 = per_expert ? 128 : p->tile_n;
   const int NM2 = per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
-  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, E, p->tile_n, per_expert, NM1, NM2,
+  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, EL, p->tile_n, per_expert, NM1, NM2,
                                   p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
                                   tiles2, ntiles2, dep, err);
   mark(2);
@@ -596,14 +604,14 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
   const unsigned gblocks = static_cast<unsigned>((gwarps * 32 + 255) / 256);
   if (p->dtype == MOE_DTYPE_F32)
-    gather_kernel<0><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
-                                              p->route_tpc, src, pos, xq, xs);
+    gather_kernel<0><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, k,
+                                              p->route_tpc, e_base, EL, src, pos, xq, xs);
   else if (p->dtype == MOE_DTYPE_BF16)
-    gather_kernel<1><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
-                                              p->route_tpc, src, pos, xq, xs);
+    gather_kernel<1><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, k,
+                                              p->route_tpc, e_base, EL, src, pos, xq, xs);
   else
-    gather_kernel<2><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, E, k,
-                                              p->route_tpc, src, pos, xq, xs);
+    gather_kernel<2><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, k,
+                                              p->route_tpc, e_base, EL, src, pos, xq, xs);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
 
@@ -615,8 +623,8 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
                                  : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                                      : CU_TENSOR_MAP_DATA_TYPE_UINT8;
   GemmMaps m1, m2;
-  bool maps_ok = make_tmap(&m1.a, w13, dt, esize, H, static_cast<uint64_t>(E) * 2 * I, 128) &&
-                 make_tmap(&m2.a, w2, dt, esize, I, static_cast<uint64_t>(E) * H, 128);
+  bool maps_ok = make_tmap(&m1.a, w13, dt, esize, H, static_cast<uint64_t>(EL) * 2 * I, 128) &&
+                 make_tmap(&m2.a, w2, dt, esize, I, static_cast<uint64_t>(EL) * H, 128);
   for (int i = 0; i < kTokMaps && maps_ok; ++i) {  // token boxes 16 .. 256 rows
     const uint32_t rows = 16u << i;
     maps_ok = make_tmap(&m1.b[i], xq, dt, esize, H, R, rows) &&
@@ -719,7 +727,14 @@ const char* moe_strerror(int code) {
 
 int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm, int force_est,
              moe_plan_t* plan) {
+  return moe_plan_ep(T, H, I, E, k, dtype, scoring, renorm, force_est, 1, 0, plan);
+}
+
+int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm,
+                int force_est, int ep_size, int ep_rank, moe_plan_t* plan) {
   if (!plan) return MOE_ERR_INVALID_ARG;
+  if (ep_size < 1 || ep_rank < 0 || ep_rank >= ep_size || E % ep_size != 0)
+    return MOE_ERR_INVALID_ARG;
   if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK ||
       force_est < 0)
     return MOE_ERR_INVALID_ARG;
@@ -745,12 +760,16 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   p.force_est = force_est;
   p.route_tpc = T > 2048 ? 32 : 8;
   p.n_chunks = (T + p.route_tpc - 1) / p.route_tpc;
+  p.ep_size = ep_size;
+  p.ep_rank = ep_rank;
+  p.e_local = E / ep_size;
+  const int EL = p.e_local;
   p.g1_mblocks = (I + 127) / 128;
   p.g2_mblocks = (H + 127) / 128;
 
   // 1) worst-case capacity, from (T, k, E, H, I, dtype) alone: the tile list
   //    is bounded with the smallest token tile (16), whatever est says
-  const long long max_tiles = (R + 15) / 16 + (E < R ? E : R) + 1;
+  const long long max_tiles = (R + 15) / 16 + (EL < R ? EL : R) + 1;
   p.max_tiles = static_cast<int32_t>(max_tiles);
   const int ex = dtype == MOE_DTYPE_F32 ? 4 : dtype == MOE_DTYPE_BF16 ? 2 : 1;
   uint64_t off = 0;
@@ -762,11 +781,11 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   p.off_err = take(16);
   p.off_ids = take(R * 4);
   p.off_w = take(R * 4);
-  p.off_chunk_counts = take(static_cast<uint64_t>(p.n_chunks) * E * 4);
+  p.off_chunk_counts = take(static_cast<uint64_t>(p.n_chunks) * EL * 4);
   p.off_lrank = take(R * 4);
-  p.off_counts = take(static_cast<uint64_t>(E) * 4);
-  p.off_offsets = take(static_cast<uint64_t>(E + 1) * 4);
-  p.off_chunk_base = take(static_cast<uint64_t>(p.n_chunks) * E * 4);
+  p.off_counts = take(static_cast<uint64_t>(EL) * 4);
+  p.off_offsets = take(static_cast<uint64_t>(EL + 1) * 4);
+  p.off_chunk_base = take(static_cast<uint64_t>(p.n_chunks) * EL * 4);
   p.off_src = take(R * 4);
   p.off_pos = take(R * 4);
   p.off_tiles = take(static_cast<uint64_t>(max_tiles) * 16);
@@ -781,7 +800,8 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
   p.off_y = take(static_cast<uint64_t>(R) * H * (dtype == MOE_DTYPE_F32 ? 4 : 2));
   p.workspace_bytes = off;
 
-  // 2) then the estimate (H20 article, para. 3) and the tile it selects
+  // 2) then the estimate (H20 article, para. 3) and the tile it selects;
+  //    the denominator is all physical experts, across expert-parallel ranks
   const long long est = force_est > 0 ? force_est : (R + E - 1) / E;
   p.est = static_cast<int32_t>(est < 1 ? 1 : est);
   p.tile_n = p.est <= 16 ? 16 : p.est <= 32 ? 32 : p.est <= 64 ? 64 : 128;
@@ -797,9 +817,11 @@ int moe_plan_describe(const moe_plan_t* p, char* buf, size_t n) {
   static const char* dn[] = {"f32", "bf16", "fp8_block128"};
   int len = std::snprintf(
       buf, buf ? n : 0,
-      "moe_plan T=%d H=%d I=%d E=%d k=%d dtype=%s scoring=%s renorm=%d est=%d%s tile_n=%d "
-      "route_tpc=%d chunks=%d max_tiles=%d g1_blocks=%d g2_blocks=%d workspace=%llu B",
-      p->T, p->H, p->I, p->E, p->k, dn[p->dtype], p->scoring ? "sigmoid" : "softmax", p->renorm,
+      "moe_plan T=%d H=%d I=%d E=%d (ep %d/%d, %d local) k=%d dtype=%s scoring=%s renorm=%d "
+      "est=%d%s tile_n=%d route_tpc=%d chunks=%d max_tiles=%d g1_blocks=%d g2_blocks=%d "
+      "workspace=%llu B",
+      p->T, p->H, p->I, p->E, p->ep_rank, p->ep_size, p->e_local, p->k, dn[p->dtype],
+      p->scoring ? "sigmoid" : "softmax", p->renorm,
       p->est, p->force_est ? " (forced)" : "", p->tile_n, p->route_tpc, p->n_chunks,
       p->max_tiles, p->g1_mblocks, p->g2_mblocks,
       static_cast<unsigned long long>(p->workspace_bytes));
@@ -843,12 +865,12 @@ int moe_route_topk(const void* logits, int logits_dtype, int T, int E, int k, in
   if (logits_dtype == MOE_LOGITS_F32)
     launch_route_t<float>(vpt_for(E), grid, 0, st, static_cast<const float*>(logits), T, E, k,
                           scoring, renorm ? 1 : 0, tpc, 0, nullptr, nullptr, ids, w, nullptr,
-                          nullptr, nullptr);
+                          nullptr, nullptr, 0, E);
   else
     launch_route_t<__nv_bfloat16>(vpt_for(E), grid, 0, st,
                                   static_cast<const __nv_bfloat16*>(logits), T, E, k, scoring,
                                   renorm ? 1 : 0, tpc, 0, nullptr, nullptr, ids, w, nullptr,
-                                  nullptr, nullptr);
+                                  nullptr, nullptr, 0, E);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

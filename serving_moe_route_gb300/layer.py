@@ -37,8 +37,11 @@ class MoELayer:
     workspace per batch size, ``forward(x, logits) -> out``."""
 
     def __init__(self, w13, w2, *, k, dtype, scoring=SOFTMAX, renorm=True, s13=None, s2=None,
-                 force_est=0):
-        E, I2, H = w13.shape
+                 force_est=0, ep_size=1, ep_rank=0):
+        """w13/w2 (and s13/s2) hold this expert-parallel rank's experts: all
+        of them when ep_size == 1, else E/ep_size of E = w13.shape[0] * ep_size;
+        forward() then returns this rank's partial sum."""
+        E, I2, H = w13.shape  # experts held by this rank
         I = I2 // 2
         _need(w13, _W_DTYPE[dtype], (E, 2 * I, H), "w13")
         _need(w2, _W_DTYPE[dtype], (E, H, I), "w2")
@@ -47,7 +50,8 @@ class MoELayer:
             _need(s2, torch.float32, (E, H // 128, I // 128), "s2")
         elif s13 is not None or s2 is not None:
             raise ValueError("block scales are only used by the FP8 layer")
-        self.E, self.H, self.I, self.k = E, H, I, k
+        self.e_local, self.E, self.H, self.I, self.k = E, E * ep_size, H, I, k
+        self.ep_size, self.ep_rank = ep_size, ep_rank
         self.dtype, self.scoring, self.renorm, self.force_est = dtype, scoring, renorm, force_est
         self.w13, self.w2, self.s13, self.s2 = w13, w2, s13, s2
         self.device = w13.device
@@ -58,8 +62,8 @@ class MoELayer:
     def plan(self, T: int) -> B.MoePlan:
         p = self._plans.get(T)
         if p is None:
-            p = B.moe_plan(T, self.H, self.I, self.E, self.k, self.dtype, self.scoring,
-                           self.renorm, self.force_est)
+            p = B.moe_plan_ep(T, self.H, self.I, self.E, self.k, self.dtype, self.scoring,
+                              self.renorm, self.force_est, self.ep_size, self.ep_rank)
             self._plans[T] = p
         return p
 
@@ -119,8 +123,8 @@ class MoELayer:
         out = {
             "ids": view(p.off_ids, R, torch.int32).view(T, self.k),
             "w": view(p.off_w, R, torch.float32).view(T, self.k),
-            "counts": view(p.off_counts, self.E, torch.int32),
-            "offsets": view(p.off_offsets, self.E + 1, torch.int32),
+            "counts": view(p.off_counts, self.e_local, torch.int32),
+            "offsets": view(p.off_offsets, self.e_local + 1, torch.int32),
             "src": view(p.off_src, R, torch.int32),
             "pos": view(p.off_pos, R, torch.int32),
             "tiles": view(p.off_tiles, p.max_tiles * 4, torch.int32).view(p.max_tiles, 4),

@@ -44,6 +44,8 @@ class Workload:
     logits: str = "normal"  # normal | router | nan_rows | concentrated | zipf
     seed: int = 0
     force_est: int = 0
+    ep_size: int = 1  # expert-parallel ranks; this workload is rank ep_rank's slice
+    ep_rank: int = 0
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
 
@@ -66,6 +68,11 @@ def workloads() -> dict:
                                                 force_est=288)
     for T in FP8_SWEEP:
         w[f"fp8_T{T}"] = _wl(f"fp8_T{T}", T, 2048, 768, 128, 8, FP8, 1003)
+    # the H20 article's setting: 400 expert slots over 8 GPUs, local MoE of one rank
+    w["sparse_uniform_bf16_ep8"] = _wl("sparse_uniform_bf16_ep8", 288, 2048, 768, 400, 6, BF16,
+                                       1002, ep_size=8)
+    w["sparse_uniform_bf16_ep8_old_est"] = _wl("sparse_uniform_bf16_ep8_old_est", 288, 2048, 768,
+                                               400, 6, BF16, 1002, ep_size=8, force_est=288)
     w["skewed_prefill_bf16"] = _wl("skewed_prefill_bf16", 4096, 2048, 768, 128, 8, BF16, 1004,
                                    logits="zipf")
     w["skewed_prefill_sigmoid_bf16"] = _wl("skewed_prefill_sigmoid_bf16", 4096, 2048, 768, 128, 8,
@@ -133,7 +140,22 @@ def make_activations(wl: Workload) -> dict:
 def make_weights(wl: Workload) -> dict:
     """w13 [E,2I,H] and w2 [E,H,I]; for the FP8 workloads float8_e4m3fn
     codes with fp32 block scales s13 [E,2I/128,H/128] and s2 [E,H/128,I/128].
-    Depends only on (H, I, E, dtype, seed), not on T."""
+    Depends only on (H, I, E, dtype, seed), not on T.  With ep_size > 1 only
+    rank ep_rank's E/ep_size experts (the same tensors as in the full set)."""
+    if wl.ep_size > 1:
+        full = make_weights(Workload(name=wl.name, T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k,
+                                     dtype=wl.dtype, seed=wl.seed)) if wl.ep_rank else None
+        el = wl.E // wl.ep_size
+        if full is None:  # rank 0: the first experts of the stream, no need for the rest
+            part = make_weights(Workload(name=wl.name, T=wl.T, H=wl.H, I=wl.I, E=el, k=wl.k,
+                                         dtype=wl.dtype, seed=wl.seed))
+            if wl.dtype == FP8:  # block scales are drawn after all codes: take them from E
+                full = make_weights(Workload(name=wl.name, T=wl.T, H=wl.H, I=wl.I, E=wl.E,
+                                             k=wl.k, dtype=wl.dtype, seed=wl.seed))
+            else:
+                return part
+        sl = slice(wl.ep_rank * el, (wl.ep_rank + 1) * el)
+        return {k2: (None if v is None else v[sl].contiguous()) for k2, v in full.items()}
     H, I, E = wl.H, wl.I, wl.E
     gw = _gen(wl.seed, 2)
     if wl.dtype in (F32, BF16):
@@ -171,10 +193,11 @@ def make_inputs(wl: Workload) -> dict:
 
 
 def custom(name="custom", *, T, H, I, E, k, dtype, scoring=SOFTMAX, renorm=True, logits="normal",
-           seed=7, force_est=0) -> Workload:
+           seed=7, force_est=0, ep_size=1, ep_rank=0) -> Workload:
     """An ad-hoc workload (edge cases in tests)."""
     return Workload(name=name, T=T, H=H, I=I, E=E, k=k, dtype=dtype, scoring=scoring,
-                    renorm=renorm, logits=logits, seed=seed, force_est=force_est)
+                    renorm=renorm, logits=logits, seed=seed, force_est=force_est,
+                    ep_size=ep_size, ep_rank=ep_rank)
 
 
 # ------------------------------------------------------------ numpy views

@@ -38,7 +38,8 @@ def make_layer(wl, inp) -> MoELayer:
     s13 = inp["s13"].to(dev) if inp["s13"] is not None else None
     s2 = inp["s2"].to(dev) if inp["s2"] is not None else None
     return MoELayer(inp["w13"].to(dev), inp["w2"].to(dev), k=wl.k, dtype=wl.dtype,
-                    scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2, force_est=wl.force_est)
+                    scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2, force_est=wl.force_est,
+                    ep_size=wl.ep_size, ep_rank=wl.ep_rank)
 
 
 def run_gpu(wl, inp, layer=None):
@@ -70,7 +71,8 @@ def run_oracle(wl, inp, tokens):
         T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, dtype=wl.dtype, scoring=wl.scoring,
         renorm=wl.renorm, x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
         w13=W.storage_numpy(inp["w13"]), w2=W.storage_numpy(inp["w2"]),
-        s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]), tokens=tokens)
+        s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]), tokens=tokens,
+        ep_size=wl.ep_size, ep_rank=wl.ep_rank)
 
 
 def check_routing_and_permutation(wl, inp, inter):

@@ -121,3 +121,16 @@ def test_forward_validates_before_launch(B):
     assert B.moe_forward(p, fake, fake, fake, fake, fake, 0, fake, fake, p.workspace_bytes,
                          0) == B.MOE_ERR_INVALID_ARG  # scales given to a bf16 layer
     assert B.moe_route_topk(fake, 1, 4, 8, 9, 0, 1, fake, fake, 0) == B.MOE_ERR_INVALID_ARG
+
+
+def test_expert_parallel_plan(B):
+    with pytest.raises(B.MoeError):
+        B.moe_plan_ep(16, 256, 128, 10, 2, B.MOE_DTYPE_BF16, ep_size=4)   # 10 % 4 != 0
+    with pytest.raises(B.MoeError):
+        B.moe_plan_ep(16, 256, 128, 16, 2, B.MOE_DTYPE_BF16, ep_size=4, ep_rank=4)
+    # the H20 article's setting: 400 slots on 8 ranks -> 50 local experts; the
+    # estimate still divides by all 400 slots
+    p = B.moe_plan_ep(288, 2048, 768, 400, 6, B.MOE_DTYPE_BF16, ep_size=8, ep_rank=3)
+    assert (p.ep_size, p.ep_rank, p.e_local, p.est) == (8, 3, 50, 5)
+    full = B.moe_plan(288, 2048, 768, 400, 6, B.MOE_DTYPE_BF16)
+    assert p.workspace_bytes < full.workspace_bytes

@@ -184,3 +184,43 @@ def test_forward_in_a_cuda_graph():
     assert torch.equal(out, eager2)
     rc, bits = layer.check(wl.T)
     assert rc == 0, bits
+
+
+@pytest.mark.parametrize("dtype", [W.BF16, W.FP8])
+def test_expert_parallel_slices(dtype):
+    # each expert-parallel rank computes its experts' share (ids global and
+    # bit-exact, local counts and permutation bit-exact, outputs against the
+    # oracle's rank slice); the ranks' outputs add up to the whole layer
+    ep, E = 4, 16
+    full_wl = W.custom("ep_full", T=60, H=256, I=128, E=E, k=3, dtype=dtype, seed=41,
+                       logits="nan_rows")
+    inp = W.make_inputs(full_wl)
+    full_out, _, _ = PU.run_gpu(full_wl, inp)
+    ids_ref, _ = oracle.route(PU.logits_f32(inp), full_wl.k)
+    flat = ids_ref.reshape(-1)
+    el = E // ep
+    total = np.zeros_like(full_out)
+    for r in range(ep):
+        wl = W.custom("ep_rank", T=60, H=256, I=128, E=E, k=3, dtype=dtype, seed=41,
+                      logits="nan_rows", ep_size=ep, ep_rank=r)
+        inp_r = dict(inp)
+        for key in ("w13", "w2", "s13", "s2"):
+            if inp[key] is not None:
+                inp_r[key] = inp[key][r * el:(r + 1) * el].contiguous()
+        out, inter, _ = PU.run_gpu(wl, inp_r)
+        np.testing.assert_array_equal(inter["ids"], ids_ref)
+        local = flat - r * el
+        valid = (local >= 0) & (local < el)
+        np.testing.assert_array_equal(inter["counts"], np.bincount(local[valid], minlength=el))
+        order = np.nonzero(valid)[0][np.argsort(local[valid], kind="stable")]
+        n_valid = int(valid.sum())
+        np.testing.assert_array_equal(inter["src"][:n_valid], order)
+        pos = np.full(flat.size, -1, np.int32)
+        pos[order] = np.arange(n_valid, dtype=np.int32)
+        np.testing.assert_array_equal(inter["pos"], pos)
+        ref, _, _ = PU.run_oracle(wl, inp_r, np.arange(wl.T, dtype=np.int32))
+        PU.check_outputs(wl, out, ref, np.arange(wl.T))
+        total += out
+    tol = PU.TOL[dtype] * np.abs(full_out).max()
+    assert np.abs(total - full_out).max() <= tol
+

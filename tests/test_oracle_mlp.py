@@ -123,3 +123,26 @@ def test_token_subset_matches_full(oracle):
     sub, ids_sub, _ = _run(oracle, wl, inp, tokens=np.array([19, 0, 7], np.int32))
     np.testing.assert_array_equal(sub, full[[19, 0, 7]])
     np.testing.assert_array_equal(ids_sub, ids_full[[19, 0, 7]])
+
+
+def test_expert_parallel_slices(oracle):
+    # one expert per rank: rank r's partial output is exactly the dense-gating
+    # term of expert r (numpy); and the ranks' partial outputs add up to the
+    # whole layer
+    wl = W.custom(T=7, H=64, I=32, E=4, k=2, dtype=W.BF16, seed=12)
+    inp = W.make_inputs(wl)
+    full, ids, w = _run(oracle, wl, inp)
+    x = _f64(inp["x"])
+    total = np.zeros_like(full)
+    for r in range(wl.E):
+        part, ids_r, w_r = oracle.moe_forward(
+            T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, dtype=wl.dtype, scoring=wl.scoring,
+            renorm=wl.renorm, x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
+            w13=W.storage_numpy(inp["w13"][r:r + 1]), w2=W.storage_numpy(inp["w2"][r:r + 1]),
+            ep_size=wl.E, ep_rank=r)
+        np.testing.assert_array_equal(ids_r, ids)
+        gate = np.where(ids == r, w, 0.0).sum(1)  # routing weight of expert r per token
+        ref = gate[:, None] * _mlp(x, _f64(inp["w13"][r]), _f64(inp["w2"][r]), wl.I)
+        np.testing.assert_allclose(part, ref, rtol=1e-9, atol=1e-12)
+        total += part
+    np.testing.assert_allclose(total, full, rtol=1e-9, atol=1e-12)
