@@ -125,7 +125,8 @@ typedef struct moe_plan {
   int32_t ep_size;    /* expert-parallel ranks (1: all experts local) */
   int32_t ep_rank;    /* this rank; it holds experts [ep_rank*e_local, +e_local) */
   int32_t e_local;    /* E / ep_size: experts in w13/w2/s13/s2 of this call */
-  int32_t reserved0;
+  int32_t n_group;    /* group-limited routing: expert groups (1 = off) */
+  int32_t topk_group; /* groups kept per token */
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;
@@ -166,6 +167,19 @@ int moe_plan(int T, int H, int I, int E, int k, int dtype, int scoring, int reno
  */
 int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm,
                 int force_est, int ep_size, int ep_rank, moe_plan_t* plan);
+
+/*
+ * moe_plan_set_groups -- switch a plan to group-limited routing: the E
+ * experts form n_group contiguous groups of E/n_group; a token keeps the
+ * topk_group groups with the largest sanitised logit (ties to the lower
+ * group) and picks its top-k among their experts only.  PR #39593 ("Test
+ * Plan") requires this grouped top-k, too, to return distinct experts for
+ * all-NaN rows; the pages do not define the grouping itself, and the group
+ * score used here (the group's best logit) is the plainest reading.
+ * Requires n_group <= 32, E % n_group == 0, 1 <= topk_group <= n_group and
+ * k <= topk_group * E / n_group; else MOE_ERR_INVALID_ARG.  Host only.
+ */
+int moe_plan_set_groups(moe_plan_t* plan, int n_group, int topk_group);
 
 /*
  * moe_forward -- steps a-1 .. a-7 for one batch, asynchronously on stream.
@@ -222,6 +236,14 @@ int moe_forward_with_ids(const moe_plan_t* plan, const void* x, const int32_t* i
  */
 int moe_route_topk(const void* logits, int logits_dtype, int T, int E, int k, int scoring,
                    int renorm, int32_t* ids, float* w, void* stream);
+
+/*
+ * moe_route_grouped_topk -- moe_route_topk with group-limited selection
+ * (see moe_plan_set_groups); n_group 1 is moe_route_topk.
+ */
+int moe_route_grouped_topk(const void* logits, int logits_dtype, int T, int E, int k,
+                           int n_group, int topk_group, int scoring, int renorm, int32_t* ids,
+                           float* w, void* stream);
 
 /*
  * moe_check -- synchronise `stream`, read the workspace error word, clear

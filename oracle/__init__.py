@@ -66,8 +66,10 @@ def lib() -> ctypes.CDLL:
         _lib.oracle_route.restype = i
         _lib.oracle_permute.argtypes = [P, i, i, P, P, P, P]
         _lib.oracle_permute.restype = i
-        _lib.oracle_moe_forward.argtypes = [i, i, i, i, i, i, i, i, i, i, P, P, P, P, P, P, P, i,
-                                            P, P, P]
+        _lib.oracle_moe_forward.argtypes = [i, i, i, i, i, i, i, i, i, i, i, i, P, P, P, P, P, P,
+                                            P, i, P, P, P]
+        _lib.oracle_route_grouped.argtypes = [P, i, i, i, i, i, i, i, P, P]
+        _lib.oracle_route_grouped.restype = i
         _lib.oracle_moe_forward.restype = i
         _lib.oracle_set_threads.argtypes = [i]
         _lib.oracle_set_threads.restype = None
@@ -127,6 +129,20 @@ def route(logits: np.ndarray, k: int, scoring: int = SOFTMAX, renorm: bool = Tru
     return ids, w
 
 
+def route_grouped(logits: np.ndarray, k: int, n_group: int, topk_group: int,
+                  scoring: int = SOFTMAX, renorm: bool = True):
+    """Group-limited routing: logits [T, E] -> (ids int32 [T, k], w float64)."""
+    logits = np.ascontiguousarray(logits, dtype=np.float32)
+    T, E = logits.shape
+    ids = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float64)
+    rc = lib().oracle_route_grouped(_ptr(logits), T, E, k, n_group, topk_group, scoring,
+                                    int(bool(renorm)), _ptr(ids), _ptr(w))
+    if rc != 0:
+        raise ValueError("oracle_route_grouped: unsupported sizes")
+    return ids, w
+
+
 def permute(ids: np.ndarray, E: int):
     """flat ids [R] -> (counts [E], offsets [E+1], src [R], pos [R]), all int32."""
     ids = np.ascontiguousarray(ids, dtype=np.int32).reshape(-1)
@@ -142,7 +158,7 @@ def permute(ids: np.ndarray, E: int):
 
 
 def moe_forward(*, T, H, I, E, k, dtype, scoring, renorm, x, logits, w13, w2, s13=None, s2=None,
-                tokens=None, ep_size=1, ep_rank=0):
+                tokens=None, ep_size=1, ep_rank=0, n_group=1, topk_group=1):
     """Fused MoE forward for the listed tokens (default: all).  With
     ep_size > 1, w13/w2/s13/s2 hold rank ep_rank's E/ep_size experts and the
     output is that rank's partial sum.
@@ -155,7 +171,7 @@ def moe_forward(*, T, H, I, E, k, dtype, scoring, renorm, x, logits, w13, w2, s1
     ids = np.empty((n, k), np.int32)
     w = np.empty((n, k), np.float64)
     rc = lib().oracle_moe_forward(
-        T, H, I, E, k, dtype, scoring, int(bool(renorm)), ep_size, ep_rank,
+        T, H, I, E, k, dtype, scoring, int(bool(renorm)), n_group, topk_group, ep_size, ep_rank,
         _ptr(x), _ptr(logits), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2),
         _ptr(tok), n, _ptr(out), _ptr(ids), _ptr(w))
     if rc != 0:

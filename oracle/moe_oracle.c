@@ -198,6 +198,70 @@ static void route_row(const float* l_in, int E, int k, int scoring, int renorm,
   }
 }
 
+/* Group-limited routing (PR #39593 "Test Plan" names a grouped top-k
+ * whose NaN rows must also give distinct experts; the pages do not define
+ * it -- reading): the E experts form n_group contiguous groups of E/n_group;
+ * a group's score is its largest sanitised logit; the topk_group best groups
+ * (ties to the lower group index) are kept, and top-k runs over the experts
+ * of the kept groups only.  Weights as route_row (softmax over all E).
+ * Only the kept groups' experts enter the final sort. */
+static void route_row_grouped(const float* l_in, int E, int k, int n_group, int topk_group,
+                              int scoring, int renorm, int32_t* ids, double* w,
+                              scored_t* scratch) {
+  const int gs = E / n_group;
+  scored_t groups[1024];
+  for (int g = 0; g < n_group; ++g) {
+    float m = -INFINITY;
+    for (int e = g * gs; e < (g + 1) * gs; ++e) m = fmaxf(m, sanitize(l_in[e]));
+    groups[g].v = m;
+    groups[g].idx = g;
+  }
+  qsort(groups, (size_t)n_group, sizeof(scored_t), cmp_scored);
+  int keep[1024] = {0};
+  for (int i = 0; i < topk_group; ++i) keep[groups[i].idx] = 1;
+  int n = 0;
+  for (int e = 0; e < E; ++e)
+    if (keep[e / gs]) {
+      scratch[n].v = sanitize(l_in[e]);
+      scratch[n].idx = e;
+      ++n;
+    }
+  qsort(scratch, (size_t)n, sizeof(scored_t), cmp_scored);
+  for (int j = 0; j < k; ++j) ids[j] = scratch[j].idx;
+  double picked[1024];
+  if (scoring == 0) {
+    double m = -INFINITY;
+    for (int e = 0; e < E; ++e) m = fmax(m, (double)sanitize(l_in[e]));
+    double z = 0.0;
+    for (int e = 0; e < E; ++e) z += exp((double)sanitize(l_in[e]) - m);
+    for (int j = 0; j < k; ++j) picked[j] = exp((double)sanitize(l_in[ids[j]]) - m) / z;
+  } else {
+    for (int j = 0; j < k; ++j)
+      picked[j] = 1.0 / (1.0 + exp(-(double)sanitize(l_in[ids[j]])));
+  }
+  double den = 0.0;
+  for (int j = 0; j < k; ++j) den += picked[j];
+  for (int j = 0; j < k; ++j)
+    w[j] = renorm ? ((den > 0.0 && isfinite(den)) ? picked[j] / den : 1.0 / (double)k)
+                  : picked[j];
+}
+
+/* Grouped routing of T tokens; requires n_group | E, 1 <= topk_group <=
+ * n_group and k <= topk_group * E / n_group.  Returns 0 or -1. */
+int oracle_route_grouped(const float* logits, int T, int E, int k, int n_group, int topk_group,
+                         int scoring, int renorm, int32_t* ids, double* w) {
+  if (T < 0 || E < 1 || E > 1024 || k < 1 || n_group < 1 || E % n_group != 0 ||
+      topk_group < 1 || topk_group > n_group || k > topk_group * (E / n_group))
+    return -1;
+  scored_t* scratch = (scored_t*)malloc(sizeof(scored_t) * (size_t)E);
+  if (!scratch) return -1;
+  for (int t = 0; t < T; ++t)
+    route_row_grouped(logits + (size_t)t * E, E, k, n_group, topk_group, scoring, renorm,
+                      ids + (size_t)t * k, w + (size_t)t * k, scratch);
+  free(scratch);
+  return 0;
+}
+
 /* Route T tokens.  logits [T, E] fp32 values (bf16 logits are widened
  * exactly by the caller).  ids [T, k], w [T, k].  Returns 0, or -1 on bad
  * sizes (k must be in [1, E], E <= 1024). */
@@ -291,6 +355,7 @@ static void fake_quant_row(const float* v, int n, double* out, uint8_t* codes, f
 
 /*
  * The fused MoE layer forward for a list of tokens.
+ * n_group > 1 selects group-limited routing (route_row_grouped).
  * Expert parallelism (H20 article, para. 2: the fused-MoE API takes the
  * expert-parallel size and rank): with ep_size > 1 the weights hold only
  * the E / ep_size experts of rank ep_rank (global ids ep_rank*E/ep_size ..
@@ -306,12 +371,16 @@ static void fake_quant_row(const float* v, int n, double* out, uint8_t* codes, f
  * (either may be NULL).  Returns 0, or -1 on unsupported sizes.
  */
 int oracle_moe_forward(int T, int H, int I, int E, int k, int dtype, int scoring, int renorm,
+                       int n_group, int topk_group,
                        int ep_size, int ep_rank, const void* x, const void* logits,
                        const void* w13, const float* s13, const void* w2, const float* s2,
                        const int32_t* tokens, int n_tokens, double* out, int32_t* ids_out,
                        double* w_out) {
   if (T < 0 || H < 1 || I < 1 || E < 1 || E > 1024 || k < 1 || k > E) return -1;
   if (ep_size < 1 || E % ep_size != 0 || ep_rank < 0 || ep_rank >= ep_size) return -1;
+  if (n_group < 1 || E % n_group != 0 || topk_group < 1 || topk_group > n_group ||
+      k > topk_group * (E / n_group))
+    return -1;
   const int e_local = E / ep_size, e_base = ep_rank * e_local;
   if (dtype == ORACLE_DTYPE_FP8 && (H % 128 != 0 || I % 128 != 0)) return -1;
   if (!tokens) n_tokens = T;
@@ -352,7 +421,10 @@ int oracle_moe_forward(int T, int H, int I, int E, int k, int dtype, int scoring
       lrow[e] = dtype == ORACLE_DTYPE_F32 ? ((const float*)logits)[i]
                                           : oracle_bf16_to_f32(((const uint16_t*)logits)[i]);
     }
-    route_row(lrow, E, k, scoring, renorm, ids, w, scratch);
+    if (n_group > 1)
+      route_row_grouped(lrow, E, k, n_group, topk_group, scoring, renorm, ids, w, scratch);
+    else
+      route_row(lrow, E, k, scoring, renorm, ids, w, scratch);
     if (ids_out)
       for (int j = 0; j < k; ++j) ids_out[(size_t)n * k + j] = ids[j];
     if (w_out)

@@ -28,7 +28,8 @@ MOE_LOGITS_F32, MOE_LOGITS_BF16 = 0, 1
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 
 EXPORTED = ("moe_plan", "moe_plan_ep", "moe_forward", "moe_forward_timed", "moe_forward_with_ids",
-            "moe_forward_noalloc", "moe_route_topk", "moe_check", "moe_plan_describe",
+            "moe_forward_noalloc", "moe_route_topk", "moe_route_grouped_topk",
+            "moe_plan_set_groups", "moe_check", "moe_plan_describe",
             "moe_strerror", "moe_abi_version")
 
 
@@ -37,7 +38,7 @@ class MoePlan(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in (
         "abi_version", "T", "H", "I", "E", "k", "dtype", "scoring", "renorm", "est", "force_est",
         "tile_n", "route_tpc", "n_chunks", "max_tiles", "g1_mblocks", "g2_mblocks", "ep_size",
-        "ep_rank", "e_local", "reserved0")]
+        "ep_rank", "e_local", "n_group", "topk_group")]
     _fields_ += [(n, c_u64) for n in (
         "workspace_bytes", "off_err", "off_ids", "off_w", "off_chunk_counts", "off_lrank",
         "off_counts", "off_offsets", "off_chunk_base", "off_src", "off_pos", "off_tiles",
@@ -98,6 +99,10 @@ def lib() -> ctypes.CDLL:
     L.moe_forward_noalloc.argtypes = [ctypes.POINTER(MoePlan), P, P, P, P, P, P, P, P]
     L.moe_forward_noalloc.restype = i
     L.moe_route_topk.argtypes = [P, i, i, i, i, i, i, P, P, P]
+    L.moe_route_grouped_topk.argtypes = [P, i, i, i, i, i, i, i, i, P, P, P]
+    L.moe_route_grouped_topk.restype = i
+    L.moe_plan_set_groups.argtypes = [ctypes.POINTER(MoePlan), i, i]
+    L.moe_plan_set_groups.restype = i
     L.moe_route_topk.restype = i
     L.moe_check.argtypes = [ctypes.POINTER(MoePlan), P, ctypes.POINTER(c_u32), P]
     L.moe_check.restype = i
@@ -162,6 +167,18 @@ def moe_forward_noalloc(plan, x, logits, w13, s13, w2, s2, out, stream):
 def moe_route_topk(logits, logits_dtype, T, E, k, scoring, renorm, ids, w, stream):
     return lib().moe_route_topk(logits, logits_dtype, T, E, k, scoring, int(bool(renorm)), ids, w,
                                 stream)
+
+
+def moe_route_grouped_topk(logits, logits_dtype, T, E, k, n_group, topk_group, scoring, renorm,
+                           ids, w, stream):
+    return lib().moe_route_grouped_topk(logits, logits_dtype, T, E, k, n_group, topk_group,
+                                        scoring, int(bool(renorm)), ids, w, stream)
+
+
+def moe_plan_set_groups(plan, n_group, topk_group):
+    _check(lib().moe_plan_set_groups(ctypes.byref(plan), n_group, topk_group),
+           "moe_plan_set_groups")
+    return plan
 
 
 def moe_check(plan, ws, stream):

@@ -56,7 +56,8 @@ __global__ void __launch_bounds__(kRouteThreads)
     route_kernel(const LT* __restrict__ logits, int T, int E, int k, int scoring, int renorm,
                  int tpc, int mode, const int* __restrict__ ids_in, const float* __restrict__ w_in,
                  int* __restrict__ ids, float* __restrict__ w, int* __restrict__ chunk_counts,
-                 int* __restrict__ lrank, unsigned* __restrict__ err, int e_base, int e_local) {
+                 int* __restrict__ lrank, unsigned* __restrict__ err, int e_base, int e_local,
+                 int n_group, int topk_group) {
   extern __shared__ int sid[];  // [tpc * k] picks of this CTA's tokens
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t0 = blockIdx.x * tpc;
@@ -74,6 +75,47 @@ __global__ void __launch_bounds__(kRouteThreads)
         v[i] = (e < E) ? sanitize_logit(load_logit(logits + static_cast<size_t>(t) * E + e)) : 0.0f;
       }
       uint32_t taken = 0;
+      if (n_group > 1) {
+        // group-limited routing: lane g holds the largest sanitised logit of
+        // group g; keep the topk_group best groups (ties to the lower group)
+        // and exclude the other groups' experts from the top-k below
+        const int gs = E / n_group;
+        float my_gmax = -INFINITY;
+        for (int g = 0; g < n_group; ++g) {
+          float m = -INFINITY;
+#pragma unroll
+          for (int i = 0; i < VPT; ++i) {
+            const int e = i * 32 + lane;
+            if (e < E && e / gs == g) m = fmaxf(m, v[i]);
+          }
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+          if (lane == g) my_gmax = m;
+        }
+        uint32_t kept = 0;
+        bool mine_kept = false;
+        for (int r = 0; r < topk_group; ++r) {
+          const bool avail = lane < n_group && !mine_kept;
+          float bv = avail ? my_gmax : -INFINITY;
+          int bi = avail ? lane : 0x7fffffff;
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (ov > bv || (ov == bv && oi < bi)) {
+              bv = ov;
+              bi = oi;
+            }
+          }
+          kept |= 1u << bi;
+          if (lane == bi) mine_kept = true;
+        }
+#pragma unroll
+        for (int i = 0; i < VPT; ++i) {
+          const int e = i * 32 + lane;
+          if (e < E && !((kept >> (e / gs)) & 1u)) taken |= 1u << i;
+        }
+      }
       float my_v = 0.0f;
       for (int j = 0; j < k; ++j) {
         float bv = -INFINITY;
@@ -438,12 +480,14 @@ template <typename LT>
 static void launch_route_t(int vpt, dim3 grid, size_t smem, cudaStream_t st, const LT* logits,
                            int T, int E, int k, int scoring, int renorm, int tpc, int mode,
                            const int* ids_in, const float* w_in, int* ids, float* w, int* cc,
-                           int* lr, unsigned* err, int e_base, int e_local) {
+                           int* lr, unsigned* err, int e_base, int e_local, int n_group = 1,
+                           int topk_group = 1) {
 #define MOE_ROUTE_CASE(V)                                                                      \
   case V:                                                                                      \
     route_kernel<V, LT><<<grid, kRouteThreads, smem, st>>>(logits, T, E, k, scoring, renorm, \
                                                            tpc, mode, ids_in, w_in, ids, w,  \
-                                                           cc, lr, err, e_base, e_local);    \
+                                                           cc, lr, err, e_base, e_local,     \
+                                                           n_group, topk_group);             \
     break;
   switch (vpt) {
     MOE_ROUTE_CASE(1)
@@ -523,7 +567,8 @@ static uint32_t tmem_cols_for(int need) {
 static int plan_ok(const moe_plan_t* p) {
   return p && p->abi_version == MOE_ABI_VERSION && p->T >= 0 && p->E >= 1 && p->k >= 1 &&
          p->tile_n >= 16 && p->ep_size >= 1 && p->e_local >= 1 &&
-         p->e_local * p->ep_size == p->E && p->ep_rank >= 0 && p->ep_rank < p->ep_size;
+         p->e_local * p->ep_size == p->E && p->ep_rank >= 0 && p->ep_rank < p->ep_size &&
+         p->n_group >= 1 && p->topk_group >= 1;
 }
 
 // the common forward; ids_in/w_in non-null selects caller-supplied routing
@@ -581,12 +626,12 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
     launch_route_t<float>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
                           static_cast<const float*>(logits), T, E, k, p->scoring, p->renorm,
                           p->route_tpc, mode, ids_in, w_in, ids, topw, chunk_counts, lrank, err,
-                          e_base, EL);
+                          e_base, EL, p->n_group, p->topk_group);
   else
     launch_route_t<__nv_bfloat16>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
                                   static_cast<const __nv_bfloat16*>(logits), T, E, k, p->scoring,
                                   p->renorm, p->route_tpc, mode, ids_in, w_in, ids, topw,
-                                  chunk_counts, lrank, err, e_base, EL);
+                                  chunk_counts, lrank, err, e_base, EL, p->n_group, p->topk_group);
   mark(1);
   // a-2 / a-3 scan and tile list
   const int per_expert = fp8 ? 0 : 1;
@@ -762,6 +807,8 @@ int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int r
   p.n_chunks = (T + p.route_tpc - 1) / p.route_tpc;
   p.ep_size = ep_size;
   p.ep_rank = ep_rank;
+  p.n_group = 1;
+  p.topk_group = 1;
   p.e_local = E / ep_size;
   const int EL = p.e_local;
   p.g1_mblocks = (I + 127) / 128;
@@ -852,9 +899,30 @@ int moe_forward_with_ids(const moe_plan_t* plan, const void* x, const int32_t* i
                       nullptr, true);
 }
 
+static bool groups_ok(int E, int k, int n_group, int topk_group) {
+  return n_group >= 1 && n_group <= 32 && E % n_group == 0 && topk_group >= 1 &&
+         topk_group <= n_group && k <= topk_group * (E / n_group);
+}
+
+int moe_plan_set_groups(moe_plan_t* plan, int n_group, int topk_group) {
+  if (!plan_ok(plan) || !groups_ok(plan->E, plan->k, n_group, topk_group))
+    return MOE_ERR_INVALID_ARG;
+  plan->n_group = n_group;
+  plan->topk_group = topk_group;
+  return MOE_OK;
+}
+
 int moe_route_topk(const void* logits, int logits_dtype, int T, int E, int k, int scoring,
                    int renorm, int32_t* ids, float* w, void* stream) {
+  return moe_route_grouped_topk(logits, logits_dtype, T, E, k, 1, 1, scoring, renorm, ids, w,
+                                stream);
+}
+
+int moe_route_grouped_topk(const void* logits, int logits_dtype, int T, int E, int k,
+                           int n_group, int topk_group, int scoring, int renorm, int32_t* ids,
+                           float* w, void* stream) {
   if (T < 0 || E < 1 || E > kMaxE || k < 1 || k > E || k > kMaxK) return MOE_ERR_INVALID_ARG;
+  if (!groups_ok(E, k, n_group, topk_group)) return MOE_ERR_INVALID_ARG;
   if (logits_dtype != MOE_LOGITS_F32 && logits_dtype != MOE_LOGITS_BF16) return MOE_ERR_INVALID_ARG;
   if (scoring != MOE_SCORING_SOFTMAX && scoring != MOE_SCORING_SIGMOID) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;  // empty batch: null pointers allowed
@@ -865,12 +933,12 @@ int moe_route_topk(const void* logits, int logits_dtype, int T, int E, int k, in
   if (logits_dtype == MOE_LOGITS_F32)
     launch_route_t<float>(vpt_for(E), grid, 0, st, static_cast<const float*>(logits), T, E, k,
                           scoring, renorm ? 1 : 0, tpc, 0, nullptr, nullptr, ids, w, nullptr,
-                          nullptr, nullptr, 0, E);
+                          nullptr, nullptr, 0, E, n_group, topk_group);
   else
     launch_route_t<__nv_bfloat16>(vpt_for(E), grid, 0, st,
                                   static_cast<const __nv_bfloat16*>(logits), T, E, k, scoring,
                                   renorm ? 1 : 0, tpc, 0, nullptr, nullptr, ids, w, nullptr,
-                                  nullptr, nullptr, 0, E);
+                                  nullptr, nullptr, 0, E, n_group, topk_group);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -37,7 +37,7 @@ class MoELayer:
     workspace per batch size, ``forward(x, logits) -> out``."""
 
     def __init__(self, w13, w2, *, k, dtype, scoring=SOFTMAX, renorm=True, s13=None, s2=None,
-                 force_est=0, ep_size=1, ep_rank=0):
+                 force_est=0, ep_size=1, ep_rank=0, n_group=1, topk_group=1):
         """w13/w2 (and s13/s2) hold this expert-parallel rank's experts: all
         of them when ep_size == 1, else E/ep_size of E = w13.shape[0] * ep_size;
         forward() then returns this rank's partial sum."""
@@ -52,6 +52,7 @@ class MoELayer:
             raise ValueError("block scales are only used by the FP8 layer")
         self.e_local, self.E, self.H, self.I, self.k = E, E * ep_size, H, I, k
         self.ep_size, self.ep_rank = ep_size, ep_rank
+        self.n_group, self.topk_group = n_group, topk_group
         self.dtype, self.scoring, self.renorm, self.force_est = dtype, scoring, renorm, force_est
         self.w13, self.w2, self.s13, self.s2 = w13, w2, s13, s2
         self.device = w13.device
@@ -64,6 +65,8 @@ class MoELayer:
         if p is None:
             p = B.moe_plan_ep(T, self.H, self.I, self.E, self.k, self.dtype, self.scoring,
                               self.renorm, self.force_est, self.ep_size, self.ep_rank)
+            if self.n_group > 1:
+                B.moe_plan_set_groups(p, self.n_group, self.topk_group)
             self._plans[T] = p
         return p
 
@@ -138,8 +141,9 @@ class MoELayer:
         return out
 
 
-def route_topk(logits, k, scoring=SOFTMAX, renorm=True, stream=None):
-    """Step a-1 alone: logits [T, E] (f32 or bf16) -> (ids int32 [T,k], w f32 [T,k])."""
+def route_topk(logits, k, scoring=SOFTMAX, renorm=True, stream=None, n_group=1, topk_group=1):
+    """Step a-1 alone: logits [T, E] (f32 or bf16) -> (ids int32 [T,k], w f32 [T,k]);
+    n_group > 1 selects group-limited routing."""
     if logits.device.type != "cuda" or not logits.is_contiguous() or logits.dim() != 2:
         raise ValueError("logits must be a contiguous 2-D CUDA tensor")
     if logits.dtype == torch.float32:
@@ -151,7 +155,7 @@ def route_topk(logits, k, scoring=SOFTMAX, renorm=True, stream=None):
     T, E = logits.shape
     ids = torch.empty(T, k, dtype=torch.int32, device=logits.device)
     w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
-    rc = B.moe_route_topk(_p(logits), ldt, T, E, k, scoring, renorm, _p(ids), _p(w),
-                          _stream(stream))
-    B._check(rc, "moe_route_topk")
+    rc = B.moe_route_grouped_topk(_p(logits), ldt, T, E, k, n_group, topk_group, scoring,
+                                  renorm, _p(ids), _p(w), _stream(stream))
+    B._check(rc, "moe_route_grouped_topk")
     return ids, w

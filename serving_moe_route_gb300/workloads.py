@@ -46,6 +46,8 @@ class Workload:
     force_est: int = 0
     ep_size: int = 1  # expert-parallel ranks; this workload is rank ep_rank's slice
     ep_rank: int = 0
+    n_group: int = 1  # group-limited routing (1 = off)
+    topk_group: int = 1
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
 
@@ -73,6 +75,9 @@ def workloads() -> dict:
                                        1002, ep_size=8)
     w["sparse_uniform_bf16_ep8_old_est"] = _wl("sparse_uniform_bf16_ep8_old_est", 288, 2048, 768,
                                                400, 6, BF16, 1002, ep_size=8, force_est=288)
+    # group-limited routing on the decode shape: 8 groups of 16, 4 kept
+    w["decode_grouped_bf16"] = _wl("decode_grouped_bf16", 128, 2048, 768, 128, 8, BF16, 1001,
+                                   logits="nan_rows", n_group=8, topk_group=4)
     w["skewed_prefill_bf16"] = _wl("skewed_prefill_bf16", 4096, 2048, 768, 128, 8, BF16, 1004,
                                    logits="zipf")
     w["skewed_prefill_sigmoid_bf16"] = _wl("skewed_prefill_sigmoid_bf16", 4096, 2048, 768, 128, 8,
@@ -193,11 +198,11 @@ def make_inputs(wl: Workload) -> dict:
 
 
 def custom(name="custom", *, T, H, I, E, k, dtype, scoring=SOFTMAX, renorm=True, logits="normal",
-           seed=7, force_est=0, ep_size=1, ep_rank=0) -> Workload:
+           seed=7, force_est=0, ep_size=1, ep_rank=0, n_group=1, topk_group=1) -> Workload:
     """An ad-hoc workload (edge cases in tests)."""
     return Workload(name=name, T=T, H=H, I=I, E=E, k=k, dtype=dtype, scoring=scoring,
                     renorm=renorm, logits=logits, seed=seed, force_est=force_est,
-                    ep_size=ep_size, ep_rank=ep_rank)
+                    ep_size=ep_size, ep_rank=ep_rank, n_group=n_group, topk_group=topk_group)
 
 
 # ------------------------------------------------------------ numpy views

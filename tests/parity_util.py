@@ -21,7 +21,7 @@ _INPUT_CACHE: dict = {}
 
 
 def inputs(wl: W.Workload) -> dict:
-    key = (wl.T, wl.H, wl.I, wl.E, wl.k, wl.dtype, wl.logits, wl.seed)
+    key = (wl.T, wl.H, wl.I, wl.E, wl.k, wl.dtype, wl.logits, wl.seed, wl.ep_size, wl.ep_rank)
     if key not in _INPUT_CACHE:
         if len(_INPUT_CACHE) > 2:
             _INPUT_CACHE.clear()
@@ -39,7 +39,8 @@ def make_layer(wl, inp) -> MoELayer:
     s2 = inp["s2"].to(dev) if inp["s2"] is not None else None
     return MoELayer(inp["w13"].to(dev), inp["w2"].to(dev), k=wl.k, dtype=wl.dtype,
                     scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2, force_est=wl.force_est,
-                    ep_size=wl.ep_size, ep_rank=wl.ep_rank)
+                    ep_size=wl.ep_size, ep_rank=wl.ep_rank, n_group=wl.n_group,
+                    topk_group=wl.topk_group)
 
 
 def run_gpu(wl, inp, layer=None):
@@ -72,18 +73,37 @@ def run_oracle(wl, inp, tokens):
         renorm=wl.renorm, x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
         w13=W.storage_numpy(inp["w13"]), w2=W.storage_numpy(inp["w2"]),
         s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]), tokens=tokens,
-        ep_size=wl.ep_size, ep_rank=wl.ep_rank)
+        ep_size=wl.ep_size, ep_rank=wl.ep_rank, n_group=wl.n_group, topk_group=wl.topk_group)
 
 
 def check_routing_and_permutation(wl, inp, inter):
     """ids / w / counts / offsets / src / pos against the oracle, all tokens."""
-    ids_ref, w_ref = oracle.route(logits_f32(inp), wl.k, scoring=wl.scoring, renorm=wl.renorm)
+    if wl.n_group > 1:
+        ids_ref, w_ref = oracle.route_grouped(logits_f32(inp), wl.k, wl.n_group, wl.topk_group,
+                                              scoring=wl.scoring, renorm=wl.renorm)
+    else:
+        ids_ref, w_ref = oracle.route(logits_f32(inp), wl.k, scoring=wl.scoring,
+                                      renorm=wl.renorm)
     np.testing.assert_array_equal(inter["ids"], ids_ref)
     np.testing.assert_allclose(inter["w"], w_ref, rtol=0, atol=W_ATOL)
-    counts, offsets, src, pos = oracle.permute(ids_ref.reshape(-1), wl.E)
+    flat = ids_ref.reshape(-1)
+    E_loc = wl.E // wl.ep_size
+    if wl.ep_size == 1:
+        counts, offsets, src, pos = oracle.permute(flat, wl.E)
+        np.testing.assert_array_equal(inter["src"], src)
+    else:
+        # an expert-parallel slice permutes only the picks of its own experts,
+        # in (local expert, flat index) order; the other picks get pos -1
+        local = flat - wl.ep_rank * E_loc
+        valid = (local >= 0) & (local < E_loc)
+        counts = np.bincount(local[valid], minlength=E_loc).astype(np.int32)
+        offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+        order = np.nonzero(valid)[0][np.argsort(local[valid], kind="stable")]
+        pos = np.full(flat.size, -1, np.int32)
+        pos[order] = np.arange(order.size, dtype=np.int32)
+        np.testing.assert_array_equal(inter["src"][:order.size], order)
     np.testing.assert_array_equal(inter["counts"], counts)
     np.testing.assert_array_equal(inter["offsets"], offsets)
-    np.testing.assert_array_equal(inter["src"], src)
     np.testing.assert_array_equal(inter["pos"], pos)
     # the tile list covers every expert's rows exactly once, in expert order,
     # each tile at most its width; the width is the plan's tile (from the
@@ -95,9 +115,9 @@ def check_routing_and_permutation(wl, inp, inter):
         lists.append(("tiles2", "ntiles2", 256))  # GEMM2's own list, widths up to 256
     for key, nkey, n_max in lists:
         nt = int(inter[nkey][0])
-        rows = np.zeros(wl.E, np.int64)
+        rows = np.zeros(E_loc, np.int64)
         for e, r0, n, width in inter[key][:nt]:
-            assert 0 <= e < wl.E and 1 <= n <= width
+            assert 0 <= e < E_loc and 1 <= n <= width
             assert offsets[e] <= r0 and r0 + n <= offsets[e + 1]
             c = counts[e]
             bucket = 16 if c <= 16 else 32 if c <= 32 else 64 if c <= 64 else 128 if c <= 128 \

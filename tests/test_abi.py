@@ -134,3 +134,25 @@ def test_expert_parallel_plan(B):
     assert (p.ep_size, p.ep_rank, p.e_local, p.est) == (8, 3, 50, 5)
     full = B.moe_plan(288, 2048, 768, 400, 6, B.MOE_DTYPE_BF16)
     assert p.workspace_bytes < full.workspace_bytes
+
+
+def test_group_limited_plan(B):
+    p = B.moe_plan(128, 2048, 768, 128, 8, B.MOE_DTYPE_BF16)
+    assert (p.n_group, p.topk_group) == (1, 1)
+    for ng, tg in [(0, 1), (3, 1), (8, 0), (8, 9), (64, 4), (8, 1)]:
+        # 0 groups; 128 % 3; no kept group; more kept than groups; >32 groups;
+        # one kept group of 16 holds k = 8 experts, so (8, 1) is valid
+        if (ng, tg) == (8, 1):
+            B.moe_plan_set_groups(p, ng, tg)
+            continue
+        with pytest.raises(B.MoeError):
+            B.moe_plan_set_groups(p, ng, tg)
+    q = B.moe_plan(16, 256, 128, 16, 8, B.MOE_DTYPE_BF16)
+    with pytest.raises(B.MoeError):   # 1 kept group of 2 experts cannot hold k = 8
+        B.moe_plan_set_groups(q, 8, 1)
+    B.moe_plan_set_groups(q, 8, 4)
+    assert (q.n_group, q.topk_group) == (8, 4)
+    fake = 256
+    assert B.moe_route_grouped_topk(fake, 0, 4, 16, 8, 8, 1, 0, 1, fake, fake, 0) == \
+        B.MOE_ERR_INVALID_ARG
+    assert B.moe_route_grouped_topk(None, 0, 0, 16, 8, 8, 4, 0, 1, None, None, 0) == B.MOE_OK

@@ -16,7 +16,8 @@ pytestmark = pytest.mark.gpu
 
 WL = W.workloads()
 
-FULL = ["tiny_f32", "decode_bf16", "sparse_uniform_bf16", "sparse_concentrated_bf16",
+FULL = ["tiny_f32", "decode_bf16", "decode_grouped_bf16", "sparse_uniform_bf16",
+        "sparse_concentrated_bf16", "sparse_uniform_bf16_ep8",
         "sparse_uniform_bf16_old_est", "fp8_T1", "fp8_T2", "fp8_T16", "fp8_T64", "fp8_T128",
         "fp8_T1024", "fp8_T4096", "skewed_prefill_bf16", "skewed_prefill_sigmoid_bf16"]
 
@@ -50,6 +51,10 @@ EDGE = [
     W.custom("big_tiles_fp8", T=300, H=256, I=256, E=4, k=2, dtype=W.FP8, seed=31),
     W.custom("forced_est", T=100, H=256, I=128, E=64, k=4, dtype=W.BF16, seed=32, force_est=100),
     W.custom("prefill_chunks", T=2500, H=128, I=128, E=32, k=4, dtype=W.BF16, seed=33),
+    W.custom("grouped_fp8", T=70, H=256, I=128, E=32, k=4, dtype=W.FP8, seed=42,
+             logits="nan_rows", n_group=8, topk_group=2),
+    W.custom("grouped_sigmoid", T=70, H=256, I=128, E=48, k=6, dtype=W.BF16, seed=43,
+             scoring=W.SIGMOID, n_group=6, topk_group=3),
 ]
 
 

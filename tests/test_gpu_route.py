@@ -75,3 +75,27 @@ def test_route_empty_and_single_token():
     lg = torch.full((1, 128), float("nan"), dtype=torch.bfloat16)
     ids = _compare(lg, 8, 0, True)
     assert list(ids[0]) == list(range(8))
+
+
+@pytest.mark.parametrize("scoring", [0, 1])
+@pytest.mark.parametrize("E,k,n_group,topk_group", [(128, 8, 8, 4), (64, 6, 4, 2), (40, 3, 8, 2),
+                                                    (256, 8, 32, 4), (16, 4, 16, 4)])
+def test_grouped_route_matches_oracle(E, k, n_group, topk_group, scoring):
+    g = torch.Generator().manual_seed(E + k + n_group)
+    T = 70
+    lg = torch.randn(T, E, generator=g)
+    lg[0] = float("nan")                      # all-NaN row: distinct, lowest groups
+    lg[1] = 0.5
+    lg[2, : E // 2] = float("nan")
+    lg[3] = torch.randint(-2, 3, (E,), generator=g).float()
+    dev = torch.device("cuda", 0)
+    for dt in (torch.float32, torch.bfloat16):
+        x = lg.to(dt)
+        ids, w = route_topk(x.to(dev), k, scoring=scoring, renorm=True, n_group=n_group,
+                            topk_group=topk_group)
+        torch.cuda.synchronize()
+        ids_ref, w_ref = oracle.route_grouped(x.float().numpy(), k, n_group, topk_group,
+                                              scoring=scoring, renorm=True)
+        np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+        np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=0, atol=2e-6)
+        assert list(ids_ref[0]) == list(range(k))

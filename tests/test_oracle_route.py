@@ -175,3 +175,61 @@ def test_permutation_concentrated_all_same_experts(oracle):
     counts, offsets, src, pos = oracle.permute(ids.reshape(-1), E)
     assert sorted(np.nonzero(counts)[0].tolist()) == [1, 3, 9, 12]
     assert np.all(counts[[1, 3, 9, 12]] == T)
+
+
+def _brute_grouped(row, k, n_group, topk_group):
+    """the unique kept-group set in which every kept group beats every other
+    group under (group max, lower group), then brute-force top-k inside"""
+    s = _sanitised(row)
+    E = len(s)
+    gs = E // n_group
+    gmax = [max(s[g * gs:(g + 1) * gs]) for g in range(n_group)]
+    found = []
+    for sub in itertools.combinations(range(n_group), topk_group):
+        if all(_beats((gmax[a], a), (gmax[b], b)) for a in sub for b in range(n_group)
+               if b not in sub):
+            found.append(sub)
+    assert len(found) == 1
+    cand = [e for e in range(E) if e // gs in found[0]]
+    best = None
+    for sub in itertools.combinations(cand, k):
+        if all(_beats((s[i], i), (s[j], j)) for i in sub for j in cand if j not in sub):
+            assert best is None
+            best = list(sub)
+    ordered = []
+    while best:
+        b = best[0]
+        for i in best[1:]:
+            if _beats((s[i], i), (s[b], b)):
+                b = i
+        ordered.append(b)
+        best.remove(b)
+    return ordered
+
+
+@pytest.mark.parametrize("E,k,n_group,topk_group", [(8, 2, 4, 2), (12, 3, 4, 2), (8, 4, 2, 1),
+                                                    (6, 2, 3, 3), (8, 1, 8, 1)])
+def test_grouped_topk_brute_force(oracle, E, k, n_group, topk_group):
+    rng = np.random.default_rng(200 + E * 10 + k + n_group)
+    logits = _rows(rng, 60, E)
+    ids, w = oracle.route_grouped(logits, k, n_group, topk_group)
+    for t in range(logits.shape[0]):
+        assert list(ids[t]) == _brute_grouped(logits[t], k, n_group, topk_group)
+        assert len(set(ids[t].tolist())) == k
+        assert abs(w[t].sum() - 1.0) < 1e-12
+
+
+def test_grouped_topk_reductions(oracle):
+    rng = np.random.default_rng(31)
+    logits = _rows(rng, 40, 16)
+    # one group, or all groups kept: plain top-k
+    for n_group, topk_group in [(1, 1), (4, 4), (16, 16)]:
+        ids_g, w_g = oracle.route_grouped(logits, 4, n_group, topk_group)
+        ids, w = oracle.route(logits, 4)
+        np.testing.assert_array_equal(ids_g, ids)
+        np.testing.assert_allclose(w_g, w, rtol=1e-15)
+    # all-NaN rows: distinct ids from the lowest groups
+    nan = np.full((2, 16), np.nan, np.float32)
+    ids, w = oracle.route_grouped(nan, 4, 4, 2)
+    assert list(ids[0]) == [0, 1, 2, 3]
+    np.testing.assert_allclose(w, 0.25)
