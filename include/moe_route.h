@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 1
+#define MOE_ABI_VERSION 2
 
 /* return codes */
 #define MOE_OK 0
@@ -127,6 +127,10 @@ typedef struct moe_plan {
   int32_t e_local;    /* E / ep_size: experts in w13/w2/s13/s2 of this call */
   int32_t n_group;    /* group-limited routing: expert groups (1 = off) */
   int32_t topk_group; /* groups kept per token */
+  int32_t gemm_pair;  /* 1: the grouped GEMMs run on CTA pairs (cta_group::2,
+                         BF16/F32 with est > 32): token tiles up to 256 rows,
+                         items of 256 weight rows; 0: one CTA per tile */
+  int32_t reserved0;
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;

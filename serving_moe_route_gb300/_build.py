@@ -1,6 +1,6 @@
 """Build step for the CUDA library: nvcc for sm_103a, in-tree.
 
-``build()`` compiles ``csrc/*.cu`` (two translation units, in parallel) and
+``build()`` compiles ``csrc/*.cu`` (one translation unit each, in parallel) and
 links ``_lib/libmoe_route.so``.  The objects go to ``_build/``.
 """
 from __future__ import annotations

@@ -39,6 +39,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include "gemm_common.cuh"
 #include "moe_internal.cuh"
 #include "ptx.cuh"
 
@@ -46,80 +47,6 @@ namespace moe {
 
 constexpr int kMaxSlots = 16;
 constexpr int kQueue = 8;  // work items handed from the producer to MMA + epilogue
-constexpr unsigned kDevErrTimeout = 4u;
-constexpr int kEpiWarps = 8;  // two column halves per TMEM lane quadrant
-constexpr int kThreads = 64 + 32 * kEpiWarps;
-
-template <int KIND>
-struct KindTraits;
-template <>
-struct KindTraits<KIND_TF32> {
-  static constexpr uint32_t fmt = 2;
-  static constexpr int esize = 4;
-};
-template <>
-struct KindTraits<KIND_BF16> {
-  static constexpr uint32_t fmt = 1;
-  static constexpr int esize = 2;
-};
-template <>
-struct KindTraits<KIND_E4M3> {
-  static constexpr uint32_t fmt = 0;
-  static constexpr int esize = 1;
-};
-
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + __expf(-z)); }
-
-// activation (GEMM1 output) and weighted expert output (GEMM2 output) stores
-template <int KIND>
-__device__ __forceinline__ void store_val(void* base, size_t idx, float v) {
-  if constexpr (KIND == KIND_TF32)
-    static_cast<float*>(base)[idx] = v;
-  else
-    static_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
-}
-
-// BF16/TF32 epilogue for C token columns starting at cc of one work item:
-// both accumulators are loaded from TMEM before one wait.  GEMM1 writes
-// act = SiLU(gate) * up; GEMM2 writes the weighted rows of one (na = 1) or
-// two (na = 2: rows row and row_b) 128-row weight tiles.
-template <int KIND, int C>
-__device__ __forceinline__ void epi_chunk(const GemmArgs& A, int g, int na, uint32_t taddr, int NM,
-                                          int cc, int row0, int nrows, int row, bool row_ok,
-                                          int row_b, bool row_b_ok, const float* cw) {
-  float v0[C], v1[C];
-  tmem_ld<C>(taddr + cc, v0);
-  if (g == 0 || na == 2) {
-    tmem_ld<C>(taddr + NM + cc, v1);
-    tmem_wait_ld(v0, v1);
-  } else {
-    tmem_wait_ld(v0);
-  }
-  if (g == 0) {
-    if (row_ok) {
-#pragma unroll
-      for (int jj = 0; jj < C; ++jj)
-        if (cc + jj < nrows)
-          store_val<KIND>(A.act, static_cast<size_t>(row0 + cc + jj) * A.I + row,
-                          silu_f(v0[jj]) * v1[jj]);
-    }
-  } else {
-    if (row_ok) {
-#pragma unroll
-      for (int jj = 0; jj < C; ++jj)
-        if (cc + jj < nrows)
-          store_val<KIND>(A.ybuf, static_cast<size_t>(row0 + cc + jj) * A.H + row,
-                          cw[cc + jj] * v0[jj]);
-    }
-    if (na == 2 && row_b_ok) {
-#pragma unroll
-      for (int jj = 0; jj < C; ++jj)
-        if (cc + jj < nrows)
-          store_val<KIND>(A.ybuf, static_cast<size_t>(row0 + cc + jj) * A.H + row_b,
-                          cw[cc + jj] * v1[jj]);
-    }
-  }
-}
 
 // Work item w of a launch: GEMM g (0 or 1), token tile t of that GEMM's
 // list, 128-row weight block mb.
@@ -127,6 +54,17 @@ struct Item {
   int g, t, mb;
   int4 tile;
 };
+
+// Token columns the MMAs of a tile compute: its rows rounded up to the MMA's
+// 16-column step, at most the tile width.  The last tile of an expert is
+// usually partly filled; computing only its rows keeps the tensor work of a
+// skewed batch close to the rows routed (the columns beyond are never read).
+template <int NT>
+__device__ __forceinline__ int mma_cols(const int4& tile) {
+  const int w = NT > 0 ? NT : tile.w;
+  const int r = (tile.z + 15) & ~15;
+  return r < w ? r : w;
+}
 
 __device__ __forceinline__ Item item_at(const GemmArgs& A, int w, int nwork1) {
   Item it;
@@ -274,10 +212,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const GemmPhase& P = args.p[I.g];
         const GemmMaps& M = I.g ? maps2 : maps1;
         const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : P.na;  // single-GEMM launches: fixed
-        const int n = NT > 0 ? NT : I.tile.w;
+        // the box: the smallest map height that holds the tile's rows
+        // rounded up to the MMA's 16-column step
+        const int nbox = 16 << tok_map_index(mma_cols<NT>(I.tile));
         const int a_row = I.tile.x * P.a_rows_per_e + I.mb * P.row_step;
-        const uint32_t tx = na * 16384u + static_cast<uint32_t>(n) * 128u;
-        const CUtensorMap* tmb = &M.b[tok_map_index(n)];  // one box of n token rows
+        const uint32_t tx = na * 16384u + static_cast<uint32_t>(nbox) * 128u;
+        const CUtensorMap* tmb = &M.b[tok_map_index(nbox)];  // one box of nbox token rows
         if (MODE == 3 && I.g == 1) {
           // this tile's activations are written by GEMM1 items of other CTAs
           if (!wait_counter(args.dep + I.t, args.p[0].mblocks, limit, abort_flag)) {
@@ -340,8 +280,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (w < 0) break;
         const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : args.p[I.g].na;
         const int kbs = args.p[I.g].kblocks;
-        const int n = NT > 0 ? NT : I.tile.w;
-        const uint32_t idesc = idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(n));
+        const uint32_t idesc =
+            idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(mma_cols<NT>(I.tile)));
         uint32_t dbase = 0, buf = 0;
         if (!FP8) {
           buf = tc % NS;
@@ -461,8 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool row_b_ok = row_b < P.m_valid;
 
       if constexpr (!FP8) {
-        const int n = I.tile.w;
-        const int hc = n / CS;  // columns per thread
+        const int n = mma_cols<NT>(I.tile);
+        const int hc = n / CS;  // columns per thread (a multiple of 8)
         const int c_begin = part * hc;
         float* cw = cs;  // GEMM2: routing weight of each token column of this tile
         if (I.g == 1) {

@@ -639,8 +639,9 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   // 2 x n-column accumulators in TMEM, so 128 is its widest double-buffered
   // tile; GEMM2 (one accumulator) widens hot experts to 256 tokens in
   // prefill-sized plans (est > 64).
-  const int NM1 = per_expert ? 128 : p->tile_n;
-  const int NM2 = per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
+  const bool pair = p->gemm_pair != 0 && !fp8;
+  const int NM1 = pair ? 256 : per_expert ? 128 : p->tile_n;
+  const int NM2 = pair ? 256 : per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
   scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, EL, p->tile_n, per_expert, NM1, NM2,
                                   p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
                                   tiles2, ntiles2, dep, err);
@@ -681,6 +682,50 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   if (sms <= 0) return MOE_ERR_CUDA;
   const int kb1 = H / (128 / esize), kb2 = I / (128 / esize);
   const int kbmax = kb1 > kb2 ? kb1 : kb2;
+  if (pair) {
+    // CTA pairs: half-height token maps, items of 256 weight rows, one
+    // token tile list (widths up to 256) for both GEMMs
+    GemmMaps h1 = m1, h2 = m2;
+    for (int i = 0; i < kTokMaps && maps_ok; ++i) {
+      const uint32_t rows = 8u << i;
+      maps_ok = make_tmap(&h1.b[i], xq, dt, esize, H, R, rows) &&
+                make_tmap(&h2.b[i], act, dt, esize, I, R, rows);
+    }
+    if (!maps_ok) return MOE_ERR_CUDA;
+    GemmArgs g{};
+    g.p[0] = GemmPhase{tiles, ntiles, 2, 256, (I + 255) / 256, kb1, 2 * I, I, I, nullptr, 0,
+                       nullptr};
+    g.p[1] = GemmPhase{tiles, ntiles, 1, 256, (H + 255) / 256, kb2, H, 128, H, nullptr, 0,
+                       nullptr};
+    g.R = static_cast<int>(R);
+    g.act = act;
+    g.I = I;
+    g.src = src;
+    g.topw = topw;
+    g.ybuf = ybuf;
+    g.H = H;
+    g.err = err;
+    g.limit_ns = kWaitLimitNs;
+    g.n_max = 256;
+    auto launch_pair = [&](int mode, const GemmMaps& maps) -> bool {
+      const int na = mode == 1 ? 2 : 1;
+      g.run1 = mode == 1;
+      g.run2 = mode == 2;
+      g.na_max = na;
+      const int budget = 227 * 1024 - kPairExtraSmem;
+      const int sb = gemm_pair_stage_bytes(na, g.n_max);
+      g.stages = budget / sb > 8 ? 8 : budget / sb;
+      g.nslots = 512 / (na * g.n_max) >= 2 ? 2 : 1;
+      g.tmem_cols = 512;
+      const int smem = g.stages * sb + kPairExtraSmem;
+      const long long items = static_cast<long long>(p->max_tiles) * g.p[mode - 1].mblocks;
+      return launch_grouped_gemm_pair(kind, mode, g, maps, smem, items, st) == cudaSuccess;
+    };
+    if (!launch_pair(1, h1)) return MOE_ERR_CUDA;
+    mark(4);
+    if (!launch_pair(2, h2)) return MOE_ERR_CUDA;
+    mark(5);
+  } else {
   GemmArgs g{};
   g.p[0] = GemmPhase{tiles, ntiles, 2, 128, p->g1_mblocks, kb1, 2 * I, I, I, s13,
                      fp8 ? 2 * I / 128 : 0, xs};
@@ -733,6 +778,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
     mark(4);
     if (!launch(0, 1, NM2, 1)) return MOE_ERR_CUDA;
     mark(5);
+  }
   }
 
   // a-7: sum of each token's k weighted rows
@@ -855,6 +901,8 @@ int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int r
   // FP8: the scale-folding epilogue keeps gate and up sums of each token
   // column in registers, which caps its tiles at 64 tokens
   if (dtype == MOE_DTYPE_FP8_BLOCK128 && p.tile_n > 64) p.tile_n = 64;
+  // experts with more than 32 rows on average: BF16/F32 GEMMs on CTA pairs
+  p.gemm_pair = (dtype != MOE_DTYPE_FP8_BLOCK128 && p.est > 32) ? 1 : 0;
   *plan = p;
   return MOE_OK;
 }

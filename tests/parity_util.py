@@ -40,7 +40,7 @@ def make_layer(wl, inp) -> MoELayer:
     return MoELayer(inp["w13"].to(dev), inp["w2"].to(dev), k=wl.k, dtype=wl.dtype,
                     scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2, force_est=wl.force_est,
                     ep_size=wl.ep_size, ep_rank=wl.ep_rank, n_group=wl.n_group,
-                    topk_group=wl.topk_group)
+                    topk_group=wl.topk_group, gemm_pair=wl.gemm_pair)
 
 
 def run_gpu(wl, inp, layer=None):
@@ -53,6 +53,7 @@ def run_gpu(wl, inp, layer=None):
     assert rc == 0, f"device error word {bits:#x}"
     inter = {k: v.cpu().numpy().copy() for k, v in layer.intermediates(wl.T).items()}
     inter["tile_n"] = layer.plan(wl.T).tile_n
+    inter["gemm_pair"] = layer.plan(wl.T).gemm_pair
     return out.float().cpu().double().numpy(), inter, layer
 
 
@@ -108,11 +109,15 @@ def check_routing_and_permutation(wl, inp, inter):
     # the tile list covers every expert's rows exactly once, in expert order,
     # each tile at most its width; the width is the plan's tile (from the
     # estimate) widened per expert to 32/64/128 by its row count (BF16/F32);
-    # GEMM2's list of a prefill-sized plan goes up to 256
+    # GEMM2's list of a prefill-sized plan goes up to 256, and CTA-pair
+    # plans share one list with widths up to 256
     tile_n = int(inter["tile_n"])
-    lists = [("tiles", "ntiles", 128)]
-    if wl.dtype != W.FP8 and tile_n >= 128:
-        lists.append(("tiles2", "ntiles2", 256))  # GEMM2's own list, widths up to 256
+    if int(inter["gemm_pair"]) and wl.dtype != W.FP8:
+        lists = [("tiles", "ntiles", 256)]
+    else:
+        lists = [("tiles", "ntiles", 128)]
+        if wl.dtype != W.FP8 and tile_n >= 128:
+            lists.append(("tiles2", "ntiles2", 256))  # GEMM2's own list, widths up to 256
     for key, nkey, n_max in lists:
         nt = int(inter[nkey][0])
         rows = np.zeros(E_loc, np.int64)

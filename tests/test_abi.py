@@ -156,3 +156,13 @@ def test_group_limited_plan(B):
     assert B.moe_route_grouped_topk(fake, 0, 4, 16, 8, 8, 1, 0, 1, fake, fake, 0) == \
         B.MOE_ERR_INVALID_ARG
     assert B.moe_route_grouped_topk(None, 0, 0, 16, 8, 8, 4, 0, 1, None, None, 0) == B.MOE_OK
+
+
+def test_plan_gemm_pair_choice(B):
+    # CTA-pair GEMMs for BF16/F32 plans whose experts average more than 32 rows
+    assert B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).gemm_pair == 1   # est 256
+    assert B.moe_plan(512, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).gemm_pair == 0    # est 32
+    assert B.moe_plan(528, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).gemm_pair == 1    # est 33
+    assert B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_FP8_BLOCK128).gemm_pair == 0
+    assert B.moe_plan(300, 160, 96, 8, 2, B.MOE_DTYPE_F32).gemm_pair == 1
+    assert B.moe_plan(288, 2048, 768, 400, 6, B.MOE_DTYPE_BF16, force_est=288).gemm_pair == 1

@@ -55,6 +55,15 @@ EDGE = [
              logits="nan_rows", n_group=8, topk_group=2),
     W.custom("grouped_sigmoid", T=70, H=256, I=128, E=48, k=6, dtype=W.BF16, seed=43,
              scoring=W.SIGMOID, n_group=6, topk_group=3),
+    # CTA-pair GEMMs: TF32; I and H not multiples of 256 (the second CTA's
+    # rows are masked in the last block); the single-CTA path forced on a
+    # prefill-sized plan and the pair path forced on a decode-sized one
+    W.custom("pair_f32", T=300, H=160, I=96, E=8, k=2, dtype=W.F32, seed=44),
+    W.custom("pair_odd_blocks", T=600, H=384, I=384, E=8, k=2, dtype=W.BF16, seed=45),
+    W.custom("single_cta_prefill", T=600, H=256, I=256, E=8, k=2, dtype=W.BF16, seed=46,
+             gemm_pair=0),
+    W.custom("pair_decode", T=64, H=256, I=256, E=32, k=4, dtype=W.BF16, seed=47,
+             logits="nan_rows", gemm_pair=1),
 ]
 
 
