@@ -37,6 +37,12 @@ struct KindTraits<KIND_E4M3> {
 // about -88 the denominator is +inf and the quotient 0, the limit of SiLU
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// two floats rounded to bf16 (nearest-even), lo in the low half
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
 // activation (GEMM1 output) and weighted expert output (GEMM2 output) stores
 template <int KIND>
 __device__ __forceinline__ void store_val(void* base, size_t idx, float v) {

@@ -21,8 +21,9 @@
 //   warp 0      TMA producer of this CTA's half of every stage; the copies
 //               of both CTAs complete on the even CTA's `full` barrier
 //   warp 1      TMEM allocation (both CTAs); MMA issue (even CTA only)
-//   warps 2..9  epilogue of this CTA's 128 rows; the drained-slot signal
-//               goes to the even CTA's `acce` barrier
+//   warps 2..17 epilogue of this CTA's 128 rows (four warps per TMEM lane
+//               quadrant, each a quarter of the token columns); the
+//               drained-slot signal goes to the even CTA's `acce` barrier
 //
 // Both CTAs walk the same item sequence (items c, c + clusters, ...).  Every
 // wait is bounded; a CTA that gives up raises the timeout bit and both CTAs
@@ -44,14 +45,21 @@ __device__ __forceinline__ int half_map_index(int h) {
   return h <= 8 ? 0 : h <= 16 ? 1 : h <= 32 ? 2 : h <= 64 ? 3 : 4;
 }
 
+// epilogue warps of a pair CTA: with a single GEMM1 accumulator slot the
+// MMAs wait for the drain, so it is spread over more warps than in the
+// single-CTA kernel
+constexpr int kPairEpiWarps = 16;
+constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;
+
 template <int KIND, int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     moe_gemm_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   constexpr int G = MODE - 1;           // which GEMM
   constexpr int NA = MODE == 1 ? 2 : 1;  // 128-row weight tiles per CTA and stage
   constexpr int BKE = 128 / KindTraits<KIND>::esize;
-  constexpr int EPI_THREADS = kEpiWarps * 32;
-  constexpr int CS = kEpiWarps / 4;  // column splits per lane quadrant
+  constexpr int EW = kPairEpiWarps;
+  constexpr int EPI_THREADS = EW * 32;
+  constexpr int CS = EW / 4;  // column parts per lane quadrant
   extern __shared__ uint8_t smem_raw[];
 
   const GemmPhase& P = args.p[G];
@@ -87,10 +95,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < NS; ++b) {
       mbar_init(smem_u32(&accf[b]), 1);
-      mbar_init(smem_u32(&acce[b]), 2 * kEpiWarps);
+      mbar_init(smem_u32(&acce[b]), 2 * EW);
     }
     mbar_init(smem_u32(done), 1);
-    mbar_init(smem_u32(epib), kEpiWarps);
+    mbar_init(smem_u32(epib), EW);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -210,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;
     const int q = warp & 3;    // TMEM lane quadrant this warp may read
-    const int part = ew >> 2;  // which half of the token columns
+    const int part = ew >> 2;  // which quarter of the token columns
     const int r_in_tile = q * 32 + lane;
     const uint32_t lane_addr = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
     const uint32_t acce_even = mapa_shared(smem_u32(acce), 0);
@@ -252,23 +260,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after();
-      const int hc = n / CS;  // columns per thread, a multiple of 8
-      const int c_begin = part * hc;
+      // this warp's share of the n columns, in whole 8-column groups
+      const int ng = n >> 3;
+      const int c_begin = ((part * ng) / CS) * 8;
+      const int c_end = (((part + 1) * ng) / CS) * 8;
       const uint32_t taddr = lane_addr + buf * slot_cols;
-      for (int c0 = 0; c0 < hc;) {
-        if (hc - c0 >= 32) {
-          epi_chunk<KIND, 32>(args, G, NA, taddr, NM, c_begin + c0, row0, nrows, row, row_ok, row,
-                              false, cw);
-          c0 += 32;
-        } else {
-          epi_chunk<KIND, 8>(args, G, NA, taddr, NM, c_begin + c0, row0, nrows, row, row_ok, row,
-                             false, cw);
-          c0 += 8;
+      if constexpr (MODE == 1 && KIND == KIND_BF16) {
+        // GEMM1 has a single accumulator slot, so the MMAs of the next item
+        // wait for it: read every column of this warp (at most 64) and
+        // reduce it to packed bf16 act first, free the slot, then store
+        uint32_t pk[32];
+        const int ncols = c_end - c_begin;
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {  // 16 columns per round
+          if (r * 16 < ncols) {        // warp-uniform
+            const int c = c_begin + r * 16;
+            float g0[8], u0[8], g1[8], u1[8];
+            tmem_ld8(taddr + c, g0);
+            tmem_ld8(taddr + NM + c, u0);
+            const bool two = r * 16 + 8 < ncols;
+            if (two) {
+              tmem_ld8(taddr + c + 8, g1);
+              tmem_ld8(taddr + NM + c + 8, u1);
+            }
+            tmem_wait_ld(g0, u0, g1, u1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              pk[r * 8 + j] = pack_bf16x2(silu_f(g0[2 * j]) * u0[2 * j],
+                                          silu_f(g0[2 * j + 1]) * u0[2 * j + 1]);
+              pk[r * 8 + 4 + j] = pack_bf16x2(silu_f(g1[2 * j]) * u1[2 * j],
+                                              silu_f(g1[2 * j + 1]) * u1[2 * j + 1]);
+            }
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_even + 8u * buf);
+        if (row_ok) {
+          __nv_bfloat16* act = static_cast<__nv_bfloat16*>(args.act);
+#pragma unroll
+          for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const int cl = r * 16 + 2 * j;  // column within this warp's share
+              const int col = c_begin + cl;
+              if (cl < ncols && col < nrows) {
+                act[static_cast<size_t>(row0 + col) * args.I + row] =
+                    __ushort_as_bfloat16(static_cast<unsigned short>(pk[r * 8 + j] & 0xffffu));
+                if (col + 1 < nrows)
+                  act[static_cast<size_t>(row0 + col + 1) * args.I + row] =
+                      __ushort_as_bfloat16(static_cast<unsigned short>(pk[r * 8 + j] >> 16));
+              }
+            }
+        }
+      } else {
+        for (int c = c_begin; c < c_end;) {
+          if (c_end - c >= 32) {
+            epi_chunk<KIND, 32>(args, G, NA, taddr, NM, c, row0, nrows, row, row_ok, row, false,
+                                cw);
+            c += 32;
+          } else {
+            epi_chunk<KIND, 8>(args, G, NA, taddr, NM, c, row0, nrows, row, row_ok, row, false,
+                               cw);
+            c += 8;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(acce_even + 8u * buf);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(acce_even + 8u * buf);
       ++tc;
     }
     if (!ok) {
@@ -305,7 +365,7 @@ static cudaError_t launch_pair_mode(const GemmArgs& args, const GemmMaps& maps, 
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(smem);
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -317,7 +377,7 @@ static cudaError_t launch_pair_mode(const GemmArgs& args, const GemmMaps& maps, 
   }
   // a persistent grid: every cluster resident at once
   const long long ncl = max_items < clusters ? (max_items > 0 ? max_items : 1) : clusters;
-  kern<<<static_cast<unsigned>(2 * ncl), kThreads, smem, stream>>>(maps, args);
+  kern<<<static_cast<unsigned>(2 * ncl), kPairThreads, smem, stream>>>(maps, args);
   return cudaGetLastError();
 }
 

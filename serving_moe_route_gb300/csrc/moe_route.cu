@@ -263,11 +263,25 @@ __device__ __forceinline__ int expert_tile(int cnt, int tile_n, int per_expert, 
 // Writes one token-tile list per grouped GEMM: list 1 with widths up to
 // n_max1 (GEMM1), list 2 up to n_max2 (GEMM2); when the caps agree list 2
 // is not written and GEMM2 reads list 1.
+// With heavy_first, the experts that fill at least one whole tile come
+// first (in expert order), then the rest: a grid-stride walk over the list
+// then deals the long items out evenly before the short ones.
 __device__ void write_tile_list(int e, int E, int cnt, int off, int ne, int max_tiles,
-                               int* warp_sums, int* tot, int4* tiles, int* ntiles,
-                               unsigned* err) {
+                               bool heavy_first, int* warp_sums, int* tot, int4* tiles,
+                               int* ntiles, unsigned* err) {
   const int ntl = (cnt + ne - 1) / ne;
-  const int tstart = block_exclusive_scan(ntl, warp_sums, tot);
+  int tstart;
+  if (heavy_first) {
+    const bool heavy = cnt >= ne;
+    __shared__ int tot_heavy;
+    const int hs = block_exclusive_scan(heavy ? ntl : 0, warp_sums, &tot_heavy);
+    const int ls = block_exclusive_scan(heavy ? 0 : ntl, warp_sums, tot);
+    tstart = heavy ? hs : tot_heavy + ls;
+    if (e == 0) *tot += tot_heavy;
+    __syncthreads();
+  } else {
+    tstart = block_exclusive_scan(ntl, warp_sums, tot);
+  }
   if (e == 0) {
     if (*tot > max_tiles) atomicOr(err, 8u);
     *ntiles = min(*tot, max_tiles);
@@ -283,7 +297,7 @@ __global__ void __launch_bounds__(1024)
                 int* __restrict__ chunk_base, int* __restrict__ counts,
                 int* __restrict__ offsets, int4* __restrict__ tiles1, int* __restrict__ ntiles1,
                 int4* __restrict__ tiles2, int* __restrict__ ntiles2, int* __restrict__ dep,
-                unsigned* __restrict__ err) {
+                int heavy_first, unsigned* __restrict__ err) {
   __shared__ int warp_sums[32];
   // fused-GEMM tile counters and the two work counters that follow them
   for (int i = threadIdx.x; i < max_tiles + 2; i += blockDim.x) dep[i] = 0;
@@ -302,10 +316,10 @@ __global__ void __launch_bounds__(1024)
   if (e < E) offsets[e] = off;
   if (e == 0) offsets[E] = tot_rows;
   write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max1), max_tiles,
-                  warp_sums, &tot_tiles1, tiles1, ntiles1, err);
+                  heavy_first, warp_sums, &tot_tiles1, tiles1, ntiles1, err);
   if (n_max2 != n_max1)
     write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max2), max_tiles,
-                    warp_sums, &tot_tiles2, tiles2, ntiles2, err);
+                    heavy_first, warp_sums, &tot_tiles2, tiles2, ntiles2, err);
 }
 
 // ------------------------------------------------------------------ gather
@@ -644,7 +658,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const int NM2 = pair ? 256 : per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
   scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, EL, p->tile_n, per_expert, NM1, NM2,
                                   p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
-                                  tiles2, ntiles2, dep, err);
+                                  tiles2, ntiles2, dep, pair ? 1 : 0, err);
   mark(2);
   // a-2 gather
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);

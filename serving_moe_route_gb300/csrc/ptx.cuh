@@ -238,6 +238,14 @@ __device__ __forceinline__ void tmem_wait_ld(float (&v)[N], float (&u)[N]) {
   for (int i = 0; i < N; ++i) asm volatile("" : "+f"(v[i]), "+f"(u[i]));
 }
 
+template <int N>
+__device__ __forceinline__ void tmem_wait_ld(float (&a)[N], float (&b)[N], float (&c)[N],
+                                             float (&d)[N]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+f"(a[i]), "+f"(b[i]), "+f"(c[i]), "+f"(d[i]));
+}
+
 // named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads)
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
