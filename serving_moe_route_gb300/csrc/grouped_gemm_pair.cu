@@ -55,7 +55,10 @@ template <int KIND, int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     moe_gemm_pair_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
   constexpr int G = MODE - 1;           // which GEMM
-  constexpr int NA = MODE == 1 ? 2 : 1;  // 128-row weight tiles per CTA and stage
+  constexpr int NA = MODE == 1 ? 2 : 1;  // 128-row weight tiles per CTA and K block
+  // K blocks (128 bytes of K each) per pipeline stage: GEMM2 takes two, so
+  // that every stage (and every commit) carries eight MMAs like GEMM1's
+  constexpr int KS = MODE == 1 ? 1 : 2;
   constexpr int BKE = 128 / KindTraits<KIND>::esize;
   constexpr int EW = kPairEpiWarps;
   constexpr int EPI_THREADS = EW * 32;
@@ -72,7 +75,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const int S = args.stages;
   const int NS = args.nslots;
   const int NM = args.n_max;  // widest pair tile (both CTAs' token rows)
-  const uint32_t stage_bytes = NA * 16384u + static_cast<uint32_t>(NM / 2) * 128u;
+  const uint32_t sub_bytes = NA * 16384u + static_cast<uint32_t>(NM / 2) * 128u;  // one K block
+  const uint32_t stage_bytes = KS * sub_bytes;
+  const int nst = (P.kblocks + KS - 1) / KS;  // stages per item (a K block past the end reads zeros)
   const uint32_t slot_cols = static_cast<uint32_t>(NA * NM);
   const uint64_t limit = args.limit_ns;
 
@@ -136,10 +141,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int mb = w % P.mblocks;
         const int h = pair_cols(tile) / 2;  // token rows of this CTA
         const int mi = half_map_index(h);
-        const uint32_t tx = NA * 16384u + (8u << mi) * 128u;  // bytes this CTA loads
+        const uint32_t tx = KS * (NA * 16384u + (8u << mi) * 128u);  // bytes this CTA loads
         const int a_row = tile.x * P.a_rows_per_e + mb * P.row_step + 128 * static_cast<int>(rank);
         const int t_row = tile.y + static_cast<int>(rank) * h;
-        for (int kb = 0; kb < P.kblocks; ++kb, ++it) {
+        for (int kb = 0; kb < nst; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (!mbar_wait(smem_u32(&empty[s]), ((it / S) & 1u) ^ 1u, limit, abort_flag)) {
             ok = false;
@@ -149,10 +154,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           const uint32_t fb = full_even + 8u * static_cast<uint32_t>(s);
           // the even CTA expects both CTAs' bytes (equal boxes on both sides)
           if (leader) mbar_arrive_expect_tx(smem_u32(&full[s]), 2u * tx);
-          const int kx = kb * BKE;
-          tma_load_2d_pair(st, &maps.a, fb, kx, a_row, pol_w);
-          if (NA == 2) tma_load_2d_pair(st + 16384u, &maps.a, fb, kx, a_row + P.a_up_off, pol_w);
-          tma_load_2d_pair(st + NA * 16384u, &maps.b[mi], fb, kx, t_row, pol_x);
+#pragma unroll
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint32_t sk = st + kk * sub_bytes;
+            const int kx = (kb * KS + kk) * BKE;
+            tma_load_2d_pair(sk, &maps.a, fb, kx, a_row, pol_w);
+            if (NA == 2)
+              tma_load_2d_pair(sk + 16384u, &maps.a, fb, kx, a_row + P.a_up_off, pol_w);
+            tma_load_2d_pair(sk + NA * 16384u, &maps.b[mi], fb, kx, t_row, pol_x);
+          }
         }
       }
       if (!ok) {
@@ -182,7 +192,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + buf * slot_cols;
-        for (int kb = 0; kb < P.kblocks; ++kb, ++it) {
+        for (int kb = 0; kb < nst; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (!mbar_wait(smem_u32(&full[s]), (it / S) & 1u, limit, abort_flag)) {
             ok = false;
@@ -190,14 +200,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
           }
           tc_fence_after();
           const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * stage_bytes);
-          const uint64_t bd0 = sdesc_sw128(sa + NA * 16384u);
 #pragma unroll
-          for (int a = 0; a < NA; ++a) {
-            const uint64_t ad0 = sdesc_sw128(sa + a * 16384u);
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint32_t sk = sa + kk * sub_bytes;
+            const uint64_t bd0 = sdesc_sw128(sk + NA * 16384u);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks)
-              mma_issue_pair<KIND>(d + a * NM, ad0 + 2u * ks, bd0 + 2u * ks, idesc,
-                                   (kb | ks) != 0);
+            for (int a = 0; a < NA; ++a) {
+              const uint64_t ad0 = sdesc_sw128(sk + a * 16384u);
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks)
+                mma_issue_pair<KIND>(d + a * NM, ad0 + 2u * ks, bd0 + 2u * ks, idesc,
+                                     (kb | kk | ks) != 0);
+            }
           }
           mma_commit_pair(smem_u32(&empty[s]), 3);  // frees the stage in both CTAs
         }

@@ -88,10 +88,13 @@ inline int gemm_extra_smem(int n_max, int kblocks_max, bool fp8) {
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& args, const GemmMaps* maps, int grid,
                                 int smem_bytes, cudaStream_t stream);
 
-// CTA-pair grouped GEMMs (BF16/TF32): one stage of one CTA holds na
-// 128-row weight tiles and half of an n_max-row token tile; the token maps
-// of `maps` are 8, 16, 32, 64 and 128 rows high (half tiles).
-inline int gemm_pair_stage_bytes(int na, int n_max) { return na * 16384 + (n_max / 2) * 128; }
+// CTA-pair grouped GEMMs (BF16/TF32): one stage of one CTA holds, for each
+// of its ks K blocks, na 128-row weight tiles and half of an n_max-row token
+// tile (GEMM1: na 2, ks 1; GEMM2: na 1, ks 2); the token maps of `maps` are
+// 8, 16, 32, 64 and 128 rows high (half tiles).
+inline int gemm_pair_stage_bytes(int na, int n_max, int ks) {
+  return ks * (na * 16384 + (n_max / 2) * 128);
+}
 constexpr int kPairExtraSmem = 3072;  // align slack, barriers, GEMM2 column weights
 
 // Launch GEMM1 (mode 1) or GEMM2 (mode 2) on CTA pairs; the grid is as many

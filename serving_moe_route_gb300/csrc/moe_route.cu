@@ -727,7 +727,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
       g.run2 = mode == 2;
       g.na_max = na;
       const int budget = 227 * 1024 - kPairExtraSmem;
-      const int sb = gemm_pair_stage_bytes(na, g.n_max);
+      const int sb = gemm_pair_stage_bytes(na, g.n_max, mode == 1 ? 1 : 2);
       g.stages = budget / sb > 8 ? 8 : budget / sb;
       g.nslots = 512 / (na * g.n_max) >= 2 ? 2 : 1;
       g.tmem_cols = 512;
