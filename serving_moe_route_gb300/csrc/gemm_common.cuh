@@ -37,6 +37,30 @@ struct KindTraits<KIND_E4M3> {
 // about -88 the denominator is +inf and the quotient 0, the limit of SiLU
 __device__ __forceinline__ float silu_f(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
+// Column maxima of a warp's C x 32 block (C columns per lane, one row per
+// lane) in 31 shuffles for C = 32: while the partner distance is at least C
+// every column is reduced; below it each step keeps half of the remaining
+// columns and trades the other half with the partner lane.  Lane l returns
+// the maximum of column (l mod C).  m[] is overwritten.
+template <int C>
+__device__ __forceinline__ float col_max_transpose(float (&m)[C], int lane) {
+#pragma unroll
+  for (int off = 16; off >= C; off >>= 1)
+#pragma unroll
+    for (int i = 0; i < C; ++i) m[i] = fmaxf(m[i], __shfl_xor_sync(0xffffffffu, m[i], off));
+#pragma unroll
+  for (int off = C / 2; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? m[i] : m[i + off];
+      const float keep = upper ? m[i + off] : m[i];
+      m[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, off));
+    }
+  }
+  return m[0];
+}
+
 // two floats rounded to bf16 (nearest-even), lo in the low half
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

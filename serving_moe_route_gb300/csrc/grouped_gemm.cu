@@ -130,7 +130,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(queue_w + kQueue);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* cs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 1024);
-  // FP8: [4][NM] per-column amax per lane quadrant (GEMM1), column weights (GEMM2)
+  // FP8: [4][NM] per-column amax per lane quadrant and [NM] reciprocal
+  // scales (GEMM1), column weights (GEMM2)
   float* red = cs + 2 * kb_max * NM;
 
   if (threadIdx.x == 0) {
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (MODE != 3) I.g = MODE - 1;
         const GemmPhase& P = args.p[I.g];
         const GemmMaps& M = I.g ? maps2 : maps1;
-        const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : P.na;  // single-GEMM launches: fixed
+        const int na = MODE == 1 ? 2 : (MODE == 2 && !FP8) ? 1 : P.na;  // single-GEMM launches: fixed
         // the box: the smallest map height that holds the tile's rows
         // rounded up to the MMA's 16-column step
         const int nbox = 16 << tok_map_index(mma_cols<NT>(I.tile));
@@ -278,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           I.g = MODE - 1;
         }
         if (w < 0) break;
-        const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : args.p[I.g].na;
+        const int na = MODE == 1 ? 2 : (MODE == 2 && !FP8) ? 1 : args.p[I.g].na;
         const int kbs = args.p[I.g].kblocks;
         const uint32_t idesc =
             idesc_make(KindTraits<KIND>::fmt, 128, static_cast<uint32_t>(mma_cols<NT>(I.tile)));
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (w < 0) break;
       const GemmPhase& P = args.p[I.g];
-      const int na = MODE == 1 ? 2 : MODE == 2 ? 1 : P.na;  // single-GEMM launches: fixed
+      const int na = MODE == 1 ? 2 : (MODE == 2 && !FP8) ? 1 : P.na;  // single-GEMM launches: fixed
       const int row0 = I.tile.y, nrows = I.tile.z;
       // output row of accumulator a: GEMM1 gate and up share a feature row;
       // GEMM2's second weight tile covers the next 128 output rows
@@ -458,15 +459,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const float* sw = P.w_scale + (static_cast<size_t>(I.tile.x) * P.w_scale_rows_per_e +
                                        I.mb * (P.row_step / 128)) * kbs;
-        for (int i = ew * 32 + lane; i < na * kbs * NT; i += EPI_THREADS) {
-          const int a = i / (kbs * NT);
-          const int kb = (i / NT) % kbs;
-          const int j = i % NT;
-          const float swv = __ldg(sw + static_cast<size_t>(a) * (P.a_up_off / 128) * kbs + kb);
-          const float* bs = P.b_scale + static_cast<size_t>(row0 + j) * kbs + kb;
-          // fused: GEMM2's scales are written in this launch, so read them
-          // through L2 (coherent) rather than the read-only path
-          cs[i] = (j < nrows) ? swv * (MODE == 3 ? __ldcg(bs) : __ldg(bs)) : 0.0f;
+        // eight products per thread and pass, their loads issued together
+        const int ncs = na * kbs * NT;
+        for (int i0 = ew * 32 + lane; i0 < ncs; i0 += 8 * EPI_THREADS) {
+          float swv[8], bsv[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * EPI_THREADS;
+            swv[u] = 0.0f;
+            bsv[u] = 0.0f;
+            if (i < ncs) {
+              const int a = i / (kbs * NT);
+              const int kb = (i / NT) % kbs;
+              const int j = i % NT;
+              if (j < nrows) {
+                swv[u] = __ldg(sw + static_cast<size_t>(a) * (P.a_up_off / 128) * kbs + kb);
+                const float* bs = P.b_scale + static_cast<size_t>(row0 + j) * kbs + kb;
+                // fused: GEMM2's scales are written in this launch, so read
+                // them through L2 (coherent) rather than the read-only path
+                bsv[u] = MODE == 3 ? __ldcg(bs) : __ldg(bs);
+              }
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int i = i0 + u * EPI_THREADS;
+            if (i < ncs) cs[i] = swv[u] * bsv[u];
+          }
         }
         if (I.g == 1)  // GEMM2: the routing weight of each token column
           for (int j = ew * 32 + lane; j < NT; j += EPI_THREADS)
@@ -494,28 +513,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dcol = (buf * GS + static_cast<uint32_t>(kb - kb0)) * slot_cols;
             const float* c0p = cs + kb * NT + c_begin;
             const float* c1p = cs + (kbs + kb) * NT + c_begin;
+            // this thread's columns of the block in chunks of up to 16, one
+            // wait per chunk
+            constexpr int FC = CPT < 16 ? CPT : 16;
 #pragma unroll
-            for (int c0 = 0; c0 < CPT; c0 += 8) {
-              float p0[8], p1[8];
-              tmem_ld8(lane_addr + dcol + c_begin + c0, p0);
+            for (int f0 = 0; f0 < CPT; f0 += FC) {
+              float p0[FC], p1[FC];
+              tmem_ld<FC>(lane_addr + dcol + c_begin + f0, p0);
               if (na == 2) {
-                tmem_ld8(lane_addr + dcol + NM + c_begin + c0, p1);
+                tmem_ld<FC>(lane_addr + dcol + NM + c_begin + f0, p1);
                 tmem_wait_ld(p0, p1);
               } else {
                 tmem_wait_ld(p0);
               }
-              const float4 s0a = *reinterpret_cast<const float4*>(c0p + c0);
-              const float4 s0b = *reinterpret_cast<const float4*>(c0p + c0 + 4);
-              const float s0[8] = {s0a.x, s0a.y, s0a.z, s0a.w, s0b.x, s0b.y, s0b.z, s0b.w};
 #pragma unroll
-              for (int jj = 0; jj < 8; ++jj) acc0[c0 + jj] = fmaf(p0[jj], s0[jj], acc0[c0 + jj]);
+              for (int c0 = 0; c0 < FC; c0 += 4) {
+                const float4 s0 = *reinterpret_cast<const float4*>(c0p + f0 + c0);
+                acc0[f0 + c0] = fmaf(p0[c0], s0.x, acc0[f0 + c0]);
+                acc0[f0 + c0 + 1] = fmaf(p0[c0 + 1], s0.y, acc0[f0 + c0 + 1]);
+                acc0[f0 + c0 + 2] = fmaf(p0[c0 + 2], s0.z, acc0[f0 + c0 + 2]);
+                acc0[f0 + c0 + 3] = fmaf(p0[c0 + 3], s0.w, acc0[f0 + c0 + 3]);
+              }
               if (na == 2) {
-                const float4 s1a = *reinterpret_cast<const float4*>(c1p + c0);
-                const float4 s1b = *reinterpret_cast<const float4*>(c1p + c0 + 4);
-                const float s1[8] = {s1a.x, s1a.y, s1a.z, s1a.w, s1b.x, s1b.y, s1b.z, s1b.w};
 #pragma unroll
-                for (int jj = 0; jj < 8; ++jj)
-                  acc1[c0 + jj] = fmaf(p1[jj], s1[jj], acc1[c0 + jj]);
+                for (int c0 = 0; c0 < FC; c0 += 4) {
+                  const float4 s1 = *reinterpret_cast<const float4*>(c1p + f0 + c0);
+                  acc1[f0 + c0] = fmaf(p1[c0], s1.x, acc1[f0 + c0]);
+                  acc1[f0 + c0 + 1] = fmaf(p1[c0 + 1], s1.y, acc1[f0 + c0 + 1]);
+                  acc1[f0 + c0 + 2] = fmaf(p1[c0 + 2], s1.z, acc1[f0 + c0 + 2]);
+                  acc1[f0 + c0 + 3] = fmaf(p1[c0 + 3], s1.w, acc1[f0 + c0 + 3]);
+                }
               }
             }
           }
@@ -526,34 +553,47 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         if (I.g == 0) {
           // act = SiLU(gate) * up, then e4m3 per token over this 128-row group
+          float m[CPT];
 #pragma unroll
           for (int c = 0; c < CPT; ++c) {
             acc0[c] = silu_f(acc0[c]) * acc1[c];
-            float m = fabsf(acc0[c]);
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1)
-              m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-            if (lane == 0) red[q * NT + c_begin + c] = m;
+            m[c] = fabsf(acc0[c]);
           }
+          // each lane ends with the maximum over this warp's 32 rows of one
+          // of the warp's columns; the four lane quadrants meet in red[]
+          const float wmax = col_max_transpose<CPT>(m, lane);
+          if (lane < CPT) red[q * NT + c_begin + lane] = wmax;
           if (!ep_barrier()) {
             ok = false;
             break;
           }
           uint8_t* act_q = static_cast<uint8_t*>(args.act);
           const int groups = args.I / 128;
+          float* inv_scale = red + 4 * NT;
+          {  // one thread per token column: the group's scale (amax / 448) and its reciprocal
+            const int j = ew * 32 + lane;
+            if (j < NT) {
+              const float amax =
+                  fmaxf(fmaxf(red[j], red[NT + j]), fmaxf(red[2 * NT + j], red[3 * NT + j]));
+              const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
+              inv_scale[j] = __frcp_rn(scale);
+              if (j < nrows) args.act_scale[static_cast<size_t>(row0 + j) * groups + I.mb] = scale;
+            }
+          }
+          if (!ep_barrier()) {
+            ok = false;
+            break;
+          }
 #pragma unroll
           for (int c = 0; c < CPT; ++c) {
             const int j = c_begin + c;
             if (j < nrows) {
-              const float amax =
-                  fmaxf(fmaxf(red[j], red[NT + j]), fmaxf(red[2 * NT + j], red[3 * NT + j]));
-              const float scale = __fdiv_rn(fmaxf(amax, 1e-10f), 448.0f);
-              float v = __fdiv_rn(acc0[c], scale);
+              // v / scale as v * (1 / scale): at most one fp32 ulp apart,
+              // far below the e4m3 step
+              float v = acc0[c] * inv_scale[j];
               v = fmaxf(fminf(v, 448.0f), -448.0f);
-              const size_t slot = static_cast<size_t>(row0 + j);
-              act_q[slot * args.I + row] =
+              act_q[static_cast<size_t>(row0 + j) * args.I + row] =
                   static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-              if (r_in_tile == 0) args.act_scale[slot * groups + I.mb] = scale;
             }
           }
         } else {

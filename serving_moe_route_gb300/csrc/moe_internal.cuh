@@ -77,11 +77,11 @@ struct GemmArgs {
 inline int gemm_stage_bytes(int na, int n_max) { return na * 16384 + n_max * 128; }
 
 // bytes of shared memory outside the stage ring (FP8: column scale products
-// of the longer K and the per-column amax exchange; otherwise GEMM2's
-// per-column weights)
+// of the longer K, the per-column amax exchange and reciprocal scales;
+// otherwise GEMM2's per-column weights)
 inline int gemm_extra_smem(int n_max, int kblocks_max, bool fp8) {
   return 1024 /* align slack */ + 1024 /* barriers, work queue, flags */ +
-         (fp8 ? 2 * n_max * kblocks_max * 4 + 4 * n_max * 4 : n_max * 4);
+         (fp8 ? 2 * n_max * kblocks_max * 4 + 5 * n_max * 4 : n_max * 4);
 }
 
 // Launch one grouped GEMM kernel (GEMM1, GEMM2 or both fused).

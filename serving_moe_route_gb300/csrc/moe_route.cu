@@ -749,8 +749,10 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   // whole, and two launches with their own stage layouts run faster.
   const bool fused = NM1 == NM2 && p->est <= 32;
   // fused GEMM2 items take two 128-row weight tiles (256 output rows), so
-  // that they stream as many weight bytes per stage as GEMM1 items
-  const int na2 = (fused && H % 256 == 0) ? 2 : 1;
+  // that they stream as many weight bytes per stage as GEMM1 items; FP8
+  // GEMM2 items do so as well, halving the per-item epilogue work (scale
+  // staging, barriers) per output row
+  const int na2 = ((fused || fp8) && H % 256 == 0) ? 2 : 1;
   const bool one_list = NM1 == NM2;  // the scan writes list 2 only when widths differ
   g.p[1] = GemmPhase{one_list ? tiles : tiles2, one_list ? ntiles : ntiles2, na2, 128 * na2,
                      (H + 128 * na2 - 1) / (128 * na2), kb2, H, 128, H, s2,
@@ -790,7 +792,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   } else {
     if (!launch(1, 0, NM1, 2)) return MOE_ERR_CUDA;
     mark(4);
-    if (!launch(0, 1, NM2, 1)) return MOE_ERR_CUDA;
+    if (!launch(0, 1, NM2, na2)) return MOE_ERR_CUDA;
     mark(5);
   }
   }
