@@ -34,7 +34,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused-MoE layer µs/call & tokens/s vs batch; % of HBM/tensor roofline, 1 GB300"
 HBM_NORTH_STAR_GBS = 8000.0
 FLUSH_BYTES = 256 << 20
-SWEEP = ["decode_bf16", "sparse_uniform_bf16", "sparse_concentrated_bf16",
+SWEEP = ["decode_bf16", "decode_grouped_bf16", "sparse_uniform_bf16", "sparse_concentrated_bf16",
          "sparse_uniform_bf16_old_est", "sparse_concentrated_bf16_old_est",
          "sparse_uniform_bf16_ep8", "sparse_uniform_bf16_ep8_old_est",
          "fp8_T1", "fp8_T2", "fp8_T4", "fp8_T16", "fp8_T64", "fp8_T128", "fp8_T256", "fp8_T1024",
@@ -188,7 +188,9 @@ class Runner:
         s2 = inp["s2"].to(dev) if inp["s2"] is not None else None
         self.layer = MoELayer(inp["w13"].to(dev), inp["w2"].to(dev), k=wl.k, dtype=wl.dtype,
                               scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2,
-                              force_est=wl.force_est, ep_size=wl.ep_size, ep_rank=wl.ep_rank)
+                              force_est=wl.force_est, ep_size=wl.ep_size, ep_rank=wl.ep_rank,
+                              n_group=wl.n_group, topk_group=wl.topk_group,
+                              gemm_pair=wl.gemm_pair)
         self.x = inp["x"].to(dev)
         self.lg = inp["logits"].to(dev)
         self.out = torch.empty(wl.T, wl.H, dtype=self.x.dtype, device=dev)
@@ -387,7 +389,8 @@ def cpu_baseline(wl, inp, seconds):
                 renorm=wl.renorm, x=W.storage_numpy(inp["x"]),
                 logits=W.storage_numpy(inp["logits"]), w13=W.storage_numpy(inp["w13"]),
                 w2=W.storage_numpy(inp["w2"]), s13=W.storage_numpy(inp["s13"]),
-                s2=W.storage_numpy(inp["s2"]), ep_size=wl.ep_size, ep_rank=wl.ep_rank)
+                s2=W.storage_numpy(inp["s2"]), ep_size=wl.ep_size, ep_rank=wl.ep_rank,
+                n_group=wl.n_group, topk_group=wl.topk_group)
     n = min(wl.T, max(1, cores))
     t0 = time.perf_counter()
     oracle.moe_forward(**args, tokens=np.arange(n, dtype=np.int32))
@@ -604,7 +607,8 @@ def run_reference(args):
               renorm=wl.renorm, x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
               w13=W.storage_numpy(inp["w13"]), w2=W.storage_numpy(inp["w2"]),
               s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]),
-              ep_size=wl.ep_size, ep_rank=wl.ep_rank)
+              ep_size=wl.ep_size, ep_rank=wl.ep_rank, n_group=wl.n_group,
+              topk_group=wl.topk_group)
     n = min(wl.T, max(1, cores))  # tokens per step: one per host core
     toks = np.arange(n, dtype=np.int32)
     for _ in range(max(0, args.warmup)):
