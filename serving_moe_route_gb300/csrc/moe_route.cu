@@ -52,18 +52,19 @@ __device__ __forceinline__ float load_logit(const __nv_bfloat16* p) {
 
 // mode 0: routing only; 1: routing + histogram; 2: validate caller ids + histogram
 template <int VPT, typename LT>
-__global__ void __launch_bounds__(kRouteThreads)
+__global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
     route_kernel(const LT* __restrict__ logits, int T, int E, int k, int scoring, int renorm,
                  int tpc, int mode, const int* __restrict__ ids_in, const float* __restrict__ w_in,
                  int* __restrict__ ids, float* __restrict__ w, int* __restrict__ chunk_counts,
                  int* __restrict__ lrank, unsigned* __restrict__ err, int e_base, int e_local,
                  int n_group, int topk_group) {
-  extern __shared__ int sid[];  // [tpc * k] picks of this CTA's tokens
+  extern __shared__ int sid[];  // [tpc * k] picks of this CTA's tokens, then [e_local] counts
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nwarps = blockDim.x >> 5;
   const int t0 = blockIdx.x * tpc;
   const int ntok = min(tpc, T - t0);
 
-  for (int tl = warp; tl < ntok; tl += kRouteThreads / 32) {
+  for (int tl = warp; tl < ntok; tl += nwarps) {
     const int t = t0 + tl;
     int my_id = -1;
     float my_w = 0.0f;
@@ -204,19 +205,25 @@ __global__ void __launch_bounds__(kRouteThreads)
   if (mode == 0) return;
   __syncthreads();
 
-  // histogram of this CTA's picks and each pick's rank among equal ids
+  // each pick's rank among the equal ids before it (a warp per pick, its
+  // lanes splitting the earlier picks), and this CTA's per-expert counts
   const int n = ntok * k;
-  for (int f = threadIdx.x; f < n; f += kRouteThreads) {
+  int* cnt = sid + tpc * k;
+  for (int e = threadIdx.x; e < e_local; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  for (int f = warp; f < n; f += nwarps) {
     const int e = sid[f];
     int r = 0;
-    for (int g = 0; g < f; ++g) r += (sid[g] == e);
-    lrank[static_cast<size_t>(t0) * k + f] = (e >= 0) ? r : -1;
+    for (int g = lane; g < f; g += 32) r += (sid[g] == e);
+    r = __reduce_add_sync(0xffffffffu, r);
+    if (lane == 0) {
+      lrank[static_cast<size_t>(t0) * k + f] = (e >= 0) ? r : -1;
+      if (e >= 0) atomicAdd(&cnt[e], 1);  // order-free: the count is exact
+    }
   }
-  for (int e = threadIdx.x; e < e_local; e += kRouteThreads) {
-    int c = 0;
-    for (int f = 0; f < n; ++f) c += (sid[f] == e);
-    chunk_counts[static_cast<size_t>(blockIdx.x) * e_local + e] = c;
-  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < e_local; e += blockDim.x)
+    chunk_counts[static_cast<size_t>(blockIdx.x) * e_local + e] = cnt[e];
 }
 
 // ------------------------------------------------------------------ scan
@@ -490,6 +497,10 @@ static int vpt_for(int E) {
   return 32;
 }
 
+// threads of a routing CTA: one warp per token of the chunk while the
+// logits of a row fit in 8 registers per lane (E <= 256), else 8 warps
+static int route_threads(int vpt, int tpc) { return vpt <= 8 ? 32 * tpc : kRouteThreads; }
+
 template <typename LT>
 static void launch_route_t(int vpt, dim3 grid, size_t smem, cudaStream_t st, const LT* logits,
                            int T, int E, int k, int scoring, int renorm, int tpc, int mode,
@@ -498,10 +509,9 @@ static void launch_route_t(int vpt, dim3 grid, size_t smem, cudaStream_t st, con
                            int topk_group = 1) {
 #define MOE_ROUTE_CASE(V)                                                                      \
   case V:                                                                                      \
-    route_kernel<V, LT><<<grid, kRouteThreads, smem, st>>>(logits, T, E, k, scoring, renorm, \
-                                                           tpc, mode, ids_in, w_in, ids, w,  \
-                                                           cc, lr, err, e_base, e_local,     \
-                                                           n_group, topk_group);             \
+    route_kernel<V, LT><<<grid, route_threads(V, tpc), smem, st>>>(                            \
+        logits, T, E, k, scoring, renorm, tpc, mode, ids_in, w_in, ids, w, cc, lr, err, e_base, \
+        e_local, n_group, topk_group);                                                         \
     break;
   switch (vpt) {
     MOE_ROUTE_CASE(1)
@@ -634,7 +644,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   mark(0);
 
   // a-1 routing (+ histogram)
-  const size_t route_smem = static_cast<size_t>(p->route_tpc) * k * sizeof(int);
+  const size_t route_smem = static_cast<size_t>(p->route_tpc * k + EL) * sizeof(int);
   const int mode = with_ids ? 2 : 1;
   if (p->dtype == MOE_DTYPE_F32)
     launch_route_t<float>(vpt_for(E), dim3(p->n_chunks), route_smem, st,
