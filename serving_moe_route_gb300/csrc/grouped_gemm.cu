@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // scales (GEMM1), column weights (GEMM2)
   float* red = cs + 2 * kb_max * NM;
 
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -171,6 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // everything above is local set-up; the tile lists and token rows are the
+  // predecessor kernels' output
+  pdl_wait();
 
   const int nwork1 = args.run1 ? (*args.p[0].ntiles) * args.p[0].mblocks : 0;
   const int nwork2 = args.run2 ? (*args.p[1].ntiles) * args.p[1].mblocks : 0;
@@ -647,8 +651,8 @@ static cudaError_t launch_mode(const GemmArgs& args, const GemmMaps* maps, int g
     if (e != cudaSuccess) return e;
     configured = smem;
   }
-  kern<<<grid, kThreads, smem, stream>>>(maps[0], maps[1], args);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(grid), dim3(kThreads), static_cast<size_t>(smem), stream,
+                        maps[0], maps[1], args);
 }
 
 template <int KIND, int NT>

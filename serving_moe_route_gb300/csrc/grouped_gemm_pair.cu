@@ -93,6 +93,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* cw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [NM]
 
+  pdl_trigger();
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);  // the even CTA's: its producer's arrival + bytes
@@ -120,6 +121,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  pdl_wait();  // the tile list and token rows are the predecessor kernels' output
 
   const int nwork = (*P.ntiles) * P.mblocks;
   int never = 0;
@@ -391,8 +393,8 @@ static cudaError_t launch_pair_mode(const GemmArgs& args, const GemmMaps& maps, 
   }
   // a persistent grid: every cluster resident at once
   const long long ncl = max_items < clusters ? (max_items > 0 ? max_items : 1) : clusters;
-  kern<<<static_cast<unsigned>(2 * ncl), kPairThreads, smem, stream>>>(maps, args);
-  return cudaGetLastError();
+  return launch_chained(kern, dim3(static_cast<unsigned>(2 * ncl)), dim3(kPairThreads),
+                        static_cast<size_t>(smem), stream, maps, args);
 }
 
 cudaError_t launch_grouped_gemm_pair(int kind, int mode, const GemmArgs& args,

@@ -84,6 +84,25 @@ inline int gemm_extra_smem(int n_max, int kblocks_max, bool fp8) {
          (fp8 ? 2 * n_max * kblocks_max * 4 + 5 * n_max * 4 : n_max * 4);
 }
 
+// Launch a kernel that may overlap its predecessor's tail in the stream
+// (programmatic dependent launch); the kernel calls pdl_wait() before it
+// touches anything the predecessor writes or reads.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_chained(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Launch one grouped GEMM kernel (GEMM1, GEMM2 or both fused).
 cudaError_t launch_grouped_gemm(int kind, const GemmArgs& args, const GemmMaps* maps, int grid,
                                 int smem_bytes, cudaStream_t stream);

@@ -29,6 +29,7 @@
 
 #include "../../include/moe_route.h"
 #include "moe_internal.cuh"
+#include "ptx.cuh"
 
 namespace moe {
 
@@ -59,6 +60,8 @@ __global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
                  int* __restrict__ lrank, unsigned* __restrict__ err, int e_base, int e_local,
                  int n_group, int topk_group) {
   extern __shared__ int sid[];  // [tpc * k] picks of this CTA's tokens, then [e_local] counts
+  pdl_trigger();
+  pdl_wait();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nwarps = blockDim.x >> 5;
   const int t0 = blockIdx.x * tpc;
@@ -306,6 +309,8 @@ __global__ void __launch_bounds__(1024)
                 int4* __restrict__ tiles2, int* __restrict__ ntiles2, int* __restrict__ dep,
                 int heavy_first, unsigned* __restrict__ err) {
   __shared__ int warp_sums[32];
+  pdl_trigger();
+  pdl_wait();
   // fused-GEMM tile counters and the two work counters that follow them
   for (int i = threadIdx.x; i < max_tiles + 2; i += blockDim.x) dep[i] = 0;
   __shared__ int tot_rows, tot_tiles1, tot_tiles2;
@@ -342,6 +347,8 @@ __global__ void __launch_bounds__(256)
                   const int* __restrict__ offsets, int T, int H, int k, int tpc, int e_base,
                   int e_local, int* __restrict__ src, int* __restrict__ pos,
                   void* __restrict__ xq, float* __restrict__ xs) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int chunks = (H + 255) / 256;
   const long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -467,6 +474,8 @@ template <typename YT>
 __global__ void __launch_bounds__(256)
     combine_kernel(const YT* __restrict__ ybuf, const int* __restrict__ pos, int T, int H, int k,
                    YT* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int chunks = (H + 255) / 256;
   const long long g = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
@@ -509,9 +518,9 @@ static void launch_route_t(int vpt, dim3 grid, size_t smem, cudaStream_t st, con
                            int topk_group = 1) {
 #define MOE_ROUTE_CASE(V)                                                                      \
   case V:                                                                                      \
-    route_kernel<V, LT><<<grid, route_threads(V, tpc), smem, st>>>(                            \
-        logits, T, E, k, scoring, renorm, tpc, mode, ids_in, w_in, ids, w, cc, lr, err, e_base, \
-        e_local, n_group, topk_group);                                                         \
+    launch_chained(route_kernel<V, LT>, grid, dim3(route_threads(V, tpc)), smem, st, logits, T, \
+                   E, k, scoring, renorm, tpc, mode, ids_in, w_in, ids, w, cc, lr, err, e_base, \
+                   e_local, n_group, topk_group);                                              \
     break;
   switch (vpt) {
     MOE_ROUTE_CASE(1)
@@ -666,22 +675,22 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const bool pair = p->gemm_pair != 0 && !fp8;
   const int NM1 = pair ? 256 : per_expert ? 128 : p->tile_n;
   const int NM2 = pair ? 256 : per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
-  scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, p->n_chunks, EL, p->tile_n, per_expert, NM1, NM2,
-                                  p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
-                                  tiles2, ntiles2, dep, pair ? 1 : 0, err);
+  launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, p->tile_n,
+                 per_expert, NM1, NM2, p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
+                 tiles2, ntiles2, dep, pair ? 1 : 0, err);
   mark(2);
   // a-2 gather
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
   const unsigned gblocks = static_cast<unsigned>((gwarps * 32 + 255) / 256);
   if (p->dtype == MOE_DTYPE_F32)
-    gather_kernel<0><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, k,
-                                              p->route_tpc, e_base, EL, src, pos, xq, xs);
+    launch_chained(gather_kernel<0>, dim3(gblocks), dim3(256), 0, st, x, ids, lrank, chunk_base,
+                   offsets, T, H, k, p->route_tpc, e_base, EL, src, pos, xq, xs);
   else if (p->dtype == MOE_DTYPE_BF16)
-    gather_kernel<1><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, k,
-                                              p->route_tpc, e_base, EL, src, pos, xq, xs);
+    launch_chained(gather_kernel<1>, dim3(gblocks), dim3(256), 0, st, x, ids, lrank, chunk_base,
+                   offsets, T, H, k, p->route_tpc, e_base, EL, src, pos, xq, xs);
   else
-    gather_kernel<2><<<gblocks, 256, 0, st>>>(x, ids, lrank, chunk_base, offsets, T, H, k,
-                                              p->route_tpc, e_base, EL, src, pos, xq, xs);
+    launch_chained(gather_kernel<2>, dim3(gblocks), dim3(256), 0, st, x, ids, lrank, chunk_base,
+                   offsets, T, H, k, p->route_tpc, e_base, EL, src, pos, xq, xs);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   mark(3);
 
@@ -811,11 +820,12 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const long long cwarps = static_cast<long long>(T) * ((H + 255) / 256);
   const unsigned cblocks = static_cast<unsigned>((cwarps * 32 + 255) / 256);
   if (p->dtype == MOE_DTYPE_F32)
-    combine_kernel<float><<<cblocks, 256, 0, st>>>(static_cast<const float*>(ybuf), pos, T, H, k,
-                                                   static_cast<float*>(out));
+    launch_chained(combine_kernel<float>, dim3(cblocks), dim3(256), 0, st,
+                   static_cast<const float*>(ybuf), pos, T, H, k, static_cast<float*>(out));
   else
-    combine_kernel<__nv_bfloat16><<<cblocks, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(ybuf), pos, T, H, k, static_cast<__nv_bfloat16*>(out));
+    launch_chained(combine_kernel<__nv_bfloat16>, dim3(cblocks), dim3(256), 0, st,
+                   static_cast<const __nv_bfloat16*>(ybuf), pos, T, H, k,
+                   static_cast<__nv_bfloat16*>(out));
   mark(6);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
