@@ -470,7 +470,9 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
   reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
 }
 
-template <typename YT>
+// RB rows' loads in flight per lane: 4 for small batches (too few warps to
+// hide the load latency otherwise), 1 when the warps alone fill the GPU
+template <typename YT, int RB>
 __global__ void __launch_bounds__(256)
     combine_kernel(const YT* __restrict__ ybuf, const int* __restrict__ pos, int T, int H, int k,
                    YT* __restrict__ out) {
@@ -482,17 +484,28 @@ __global__ void __launch_bounds__(256)
   if (g >= static_cast<long long>(T) * chunks) return;
   const int t = static_cast<int>(g / chunks);
   const int h0 = static_cast<int>(g % chunks) * 256 + lane * 8;
-  if (h0 >= H) return;
+  const bool active = h0 < H;
+  // the token's k rows: positions read once per warp, then RB rows' loads
+  // in flight at a time; the sum keeps pick order
+  const int my_pos = lane < k ? __ldg(pos + static_cast<size_t>(t) * k + lane) : -1;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int j = 0; j < k; ++j) {
-    const int p = __ldg(pos + static_cast<size_t>(t) * k + j);
-    if (p < 0) continue;
-    float v[8];
-    load8(ybuf + static_cast<size_t>(p) * H + h0, v);
+  for (int j0 = 0; j0 < k; j0 += RB) {
+    float v[RB][8];
+    bool use[RB];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += v[i];
+    for (int u = 0; u < RB; ++u) {
+      const int p = __shfl_sync(0xffffffffu, my_pos, (j0 + u) & 31);
+      use[u] = active && j0 + u < k && p >= 0;
+      if (use[u]) load8(ybuf + static_cast<size_t>(p) * H + h0, v[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < RB; ++u)
+      if (use[u]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += v[u][i];
+      }
   }
-  store8(out + static_cast<size_t>(t) * H + h0, acc);
+  if (active) store8(out + static_cast<size_t>(t) * H + h0, acc);
 }
 
 // ------------------------------------------------------------------ host helpers
@@ -820,12 +833,13 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const long long cwarps = static_cast<long long>(T) * ((H + 255) / 256);
   const unsigned cblocks = static_cast<unsigned>((cwarps * 32 + 255) / 256);
   if (p->dtype == MOE_DTYPE_F32)
-    launch_chained(combine_kernel<float>, dim3(cblocks), dim3(256), 0, st,
-                   static_cast<const float*>(ybuf), pos, T, H, k, static_cast<float*>(out));
+    launch_chained(T <= 512 ? combine_kernel<float, 4> : combine_kernel<float, 1>, dim3(cblocks),
+                   dim3(256), 0, st, static_cast<const float*>(ybuf), pos, T, H, k,
+                   static_cast<float*>(out));
   else
-    launch_chained(combine_kernel<__nv_bfloat16>, dim3(cblocks), dim3(256), 0, st,
-                   static_cast<const __nv_bfloat16*>(ybuf), pos, T, H, k,
-                   static_cast<__nv_bfloat16*>(out));
+    launch_chained(T <= 512 ? combine_kernel<__nv_bfloat16, 4> : combine_kernel<__nv_bfloat16, 1>,
+                   dim3(cblocks), dim3(256), 0, st, static_cast<const __nv_bfloat16*>(ybuf), pos,
+                   T, H, k, static_cast<__nv_bfloat16*>(out));
   mark(6);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
