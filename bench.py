@@ -57,24 +57,54 @@ def parse():
     return ap.parse_args()
 
 
-def ncu_traffic(workload):
-    """DRAM bytes (read + write) per launch of the dominant GEMM kernel from
-    the committed ncu summary, if it was taken from the current kernel
-    sources; else None."""
+def strip_c_comments(text):
+    """C/C++ source without comments and with runs of whitespace collapsed,
+    so that comment-only edits leave the code's fingerprint unchanged."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":  # string or character literal, copied as is
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return " ".join("".join(out).split())
+
+
+def kernel_source_fingerprint():
+    """sha256 over the CUDA sources (csrc/*.cu, *.cuh) with comments removed."""
     import glob
     import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "serving_moe_route_gb300", "csrc")
+    for fn in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
+        with open(fn, encoding="utf-8") as f:
+            h.update(strip_c_comments(f.read()).encode())
+    return h.hexdigest()
+
+
+def ncu_traffic(workload):
+    """DRAM bytes (read + write) per launch of the dominant GEMM kernel from
+    the committed ncu summary, if it was taken from the current kernel code
+    (the comment-free source fingerprint matches); else None."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "serving_moe_route_gb300", "csrc")
-    for fn in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
-        with open(fn, "rb") as f:
-            h.update(f.read())
     e = d.get("entries", {}).get(workload)
-    if e is None or d.get("source_sha256") != h.hexdigest():
+    if e is None or d.get("source_sha256") != kernel_source_fingerprint():
         return None
     return int(e["dram_read_bytes"] + e["dram_write_bytes"])
 

@@ -94,7 +94,9 @@ extern "C" {
  *                           ascending flat index within an expert)
  *   pos     int32 [T*k]     flat index -> permuted row (inverse of src)
  *   tiles   int32 [max_tiles, 4]  {expert, first row, rows, width} token
- *                           tiles of grouped GEMM 1, in expert order
+ *                           tiles of grouped GEMM 1, in expert order (CTA-pair
+ *                           plans: experts that fill a whole 256-row tile
+ *                           first, then the rest, each group in expert order)
  *   ntiles  int32 [1]       number of valid tiles
  *   tiles2, ntiles2         the same for grouped GEMM 2 when its widths differ
  *                           (prefill-sized BF16/F32 plans); otherwise unused
@@ -113,15 +115,18 @@ typedef struct moe_plan {
   int32_t dtype, scoring, renorm;
   int32_t est;        /* rows-per-expert estimate used for the tile choice */
   int32_t force_est;  /* 0, or the caller's override (e.g. T: old estimate) */
-  int32_t tile_n;     /* token tile = MMA N (16, 32, 64 or 128) from est; the
-                         device widens it per expert for BF16/F32 (an expert
-                         with more rows gets 32 / 64 / 128, and for grouped
-                         GEMM 2 256 when est > 64) */
+  int32_t tile_n;     /* token tile (16, 32, 64 or 128; FP8 at most 64) from
+                         est; the device widens it per expert for BF16/F32 (an
+                         expert with more rows gets 32 / 64 / 128, for grouped
+                         GEMM 2 256 when est > 64, and up to 256 for both GEMMs
+                         in CTA-pair plans).  The MMAs of a tile compute its
+                         rows rounded up to 16. */
   int32_t route_tpc;  /* tokens per routing CTA */
   int32_t n_chunks;   /* routing CTAs = ceil(T / route_tpc) */
   int32_t max_tiles;  /* worst-case token tiles (independent of est) */
-  int32_t g1_mblocks; /* ceil(I / 128) gate+up feature blocks */
-  int32_t g2_mblocks; /* ceil(H / 128) output feature blocks */
+  int32_t g1_mblocks; /* ceil(I / 128) gate+up feature blocks (CTA pairs take
+                         256 features per work item) */
+  int32_t g2_mblocks; /* ceil(H / 128) output feature blocks (CTA pairs: 256) */
   int32_t ep_size;    /* expert-parallel ranks (1: all experts local) */
   int32_t ep_rank;    /* this rank; it holds experts [ep_rank*e_local, +e_local) */
   int32_t e_local;    /* E / ep_size: experts in w13/w2/s13/s2 of this call */
@@ -129,7 +134,9 @@ typedef struct moe_plan {
   int32_t topk_group; /* groups kept per token */
   int32_t gemm_pair;  /* 1: the grouped GEMMs run on CTA pairs (cta_group::2,
                          BF16/F32 with est > 32): token tiles up to 256 rows,
-                         items of 256 weight rows; 0: one CTA per tile */
+                         items of 256 weight rows; 0: one CTA per tile.  Set by
+                         moe_plan; a caller may clear or set it (ignored for
+                         FP8). */
   int32_t reserved0;
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;

@@ -681,10 +681,11 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   mark(1);
   // a-2 / a-3 scan and tile list
   const int per_expert = fp8 ? 0 : 1;
-  // the largest tile the device may choose per GEMM.  GEMM1 keeps two
-  // 2 x n-column accumulators in TMEM, so 128 is its widest double-buffered
-  // tile; GEMM2 (one accumulator) widens hot experts to 256 tokens in
-  // prefill-sized plans (est > 64).
+  // the largest tile the device may choose per GEMM.  One CTA per tile:
+  // GEMM1 keeps two 2 x n-column accumulators in TMEM, so 128 is its widest
+  // double-buffered tile; GEMM2 (one accumulator) widens hot experts to 256
+  // tokens in prefill-sized plans (est > 64).  CTA pairs: 256 for both
+  // (each CTA holds half of the tile's rows).
   const bool pair = p->gemm_pair != 0 && !fp8;
   const int NM1 = pair ? 256 : per_expert ? 128 : p->tile_n;
   const int NM2 = pair ? 256 : per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;

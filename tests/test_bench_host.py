@@ -1,0 +1,46 @@
+"""Host-side helpers of bench.py (no GPU): the comment-free source
+fingerprint that ties the committed ncu traffic figures to the kernel code,
+and the algorithmic byte/FLOP accounting."""
+import os
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from serving_moe_route_gb300 import workloads as W  # noqa: E402
+
+
+def test_strip_c_comments_keeps_code_and_strings():
+    src = 'int a = 1; // note\n/* block\n comment */ asm("x // not a comment");\nchar c = \'/\';'
+    assert bench.strip_c_comments(src) == 'int a = 1; asm("x // not a comment"); char c = \'/\';'
+
+
+def test_fingerprint_ignores_comments_only():
+    a = "__global__ void k(int* p) { p[0] = 1; }"
+    b = "// header\n__global__ void k(int* p) {  /* store */ p[0] = 1; }\n"
+    c = "__global__ void k(int* p) { p[0] = 2; }"
+    assert bench.strip_c_comments(a) == bench.strip_c_comments(b)
+    assert bench.strip_c_comments(a) != bench.strip_c_comments(c)
+
+
+def test_committed_traffic_matches_current_kernels():
+    # the profiles/ncu_traffic.json figures come from the kernels as they
+    # stand; after a kernel change without a new capture the bench reports
+    # traffic null, and this test says so
+    import pytest
+    if bench.ncu_traffic("decode_bf16") is None:
+        pytest.skip("kernel code changed since the committed ncu traffic capture")
+    assert bench.ncu_traffic("decode_bf16") > 1_200_000_000  # the touched weights, read once
+
+
+def test_algorithmic_accounting_decode():
+    wl = W.workloads()["decode_bf16"]
+    counts = [8] * wl.E  # every expert touched
+    acc = bench.algorithmic(wl, counts)
+    assert acc["flops"] == 6.0 * 128 * 8 * 2048 * 768
+    assert acc["w13_bytes_per_expert"] == 2 * 768 * 2048 * 2
+    assert acc["w2_bytes_per_expert"] == 2048 * 768 * 2
+    assert acc["touched"] == 128
+    # layer bytes: touched weights + logits + x + out
+    assert acc["layer_bytes"] == 128 * (6291456 + 3145728) + 128 * 128 * 2 + 2 * 128 * 2048 * 2
