@@ -680,15 +680,21 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
                                   chunk_counts, lrank, err, e_base, EL, p->n_group, p->topk_group);
   mark(1);
   // a-2 / a-3 scan and tile list
-  const int per_expert = fp8 ? 0 : 1;
+  // FP8 kernels are specialised per tile width.  When experts average more
+  // than half the plan's tile (est > tile_n / 2, so that many hold more
+  // rows than the tile), the kernel is one size wider (at most 64) and each
+  // expert's tile grows to the rows it holds: fewer tiles, each weight block
+  // streamed once per expert instead of once per tile.
+  const int fp8_nt = (fp8 && 2 * p->est > p->tile_n && p->tile_n < 64) ? 2 * p->tile_n : p->tile_n;
+  const int per_expert = fp8 ? (fp8_nt > p->tile_n ? 1 : 0) : 1;
   // the largest tile the device may choose per GEMM.  One CTA per tile:
   // GEMM1 keeps two 2 x n-column accumulators in TMEM, so 128 is its widest
   // double-buffered tile; GEMM2 (one accumulator) widens hot experts to 256
   // tokens in prefill-sized plans (est > 64).  CTA pairs: 256 for both
   // (each CTA holds half of the tile's rows).
   const bool pair = p->gemm_pair != 0 && !fp8;
-  const int NM1 = pair ? 256 : per_expert ? 128 : p->tile_n;
-  const int NM2 = pair ? 256 : per_expert ? (p->tile_n >= 128 ? 256 : 128) : p->tile_n;
+  const int NM1 = pair ? 256 : fp8 ? fp8_nt : 128;
+  const int NM2 = pair ? 256 : fp8 ? fp8_nt : (p->tile_n >= 128 ? 256 : 128);
   launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, p->tile_n,
                  per_expert, NM1, NM2, p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
                  tiles2, ntiles2, dep, pair ? 1 : 0, err);

@@ -54,6 +54,7 @@ def run_gpu(wl, inp, layer=None):
     inter = {k: v.cpu().numpy().copy() for k, v in layer.intermediates(wl.T).items()}
     inter["tile_n"] = layer.plan(wl.T).tile_n
     inter["gemm_pair"] = layer.plan(wl.T).gemm_pair
+    inter["est"] = layer.plan(wl.T).est
     return out.float().cpu().double().numpy(), inter, layer
 
 
@@ -112,8 +113,14 @@ def check_routing_and_permutation(wl, inp, inter):
     # GEMM2's list of a prefill-sized plan goes up to 256, and CTA-pair
     # plans share one list with widths up to 256
     tile_n = int(inter["tile_n"])
+    # FP8: the kernel width is the plan's tile, or twice it (at most 64) when
+    # experts average more than half a tile; then widths grow per expert too
+    est = int(inter["est"])
+    fp8_nt = 2 * tile_n if (2 * est > tile_n and tile_n < 64) else tile_n
     if int(inter["gemm_pair"]) and wl.dtype != W.FP8:
         lists = [("tiles", "ntiles", 256)]
+    elif wl.dtype == W.FP8:
+        lists = [("tiles", "ntiles", fp8_nt)]
     else:
         lists = [("tiles", "ntiles", 128)]
         if wl.dtype != W.FP8 and tile_n >= 128:
@@ -127,7 +134,10 @@ def check_routing_and_permutation(wl, inp, inter):
             c = counts[e]
             bucket = 16 if c <= 16 else 32 if c <= 32 else 64 if c <= 64 else 128 if c <= 128 \
                 else 256
-            want = tile_n if wl.dtype == W.FP8 else min(n_max, max(tile_n, bucket))
+            if wl.dtype == W.FP8 and fp8_nt == tile_n:
+                want = tile_n
+            else:
+                want = min(n_max, max(tile_n, bucket))
             assert width == want, (key, e, c, width, want)
             rows[e] += n
         np.testing.assert_array_equal(rows, counts)

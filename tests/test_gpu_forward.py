@@ -19,7 +19,7 @@ WL = W.workloads()
 FULL = ["tiny_f32", "decode_bf16", "decode_grouped_bf16", "sparse_uniform_bf16",
         "sparse_concentrated_bf16", "sparse_uniform_bf16_ep8",
         "sparse_uniform_bf16_old_est", "fp8_T1", "fp8_T2", "fp8_T16", "fp8_T64", "fp8_T128",
-        "fp8_T1024", "fp8_T4096", "skewed_prefill_bf16", "skewed_prefill_sigmoid_bf16"]
+        "fp8_T256", "fp8_T1024", "fp8_T4096", "skewed_prefill_bf16", "skewed_prefill_sigmoid_bf16"]
 
 
 @pytest.mark.parametrize("name", FULL)
@@ -64,6 +64,11 @@ EDGE = [
              gemm_pair=0),
     W.custom("pair_decode", T=64, H=256, I=256, E=32, k=4, dtype=W.BF16, seed=47,
              logits="nan_rows", gemm_pair=1),
+    # FP8 with experts averaging more than half a tile: the kernel one width
+    # up and per-expert widths (est 12 -> 32-wide kernel; est 24 -> 64)
+    W.custom("fp8_wider_32", T=96, H=256, I=256, E=32, k=4, dtype=W.FP8, seed=48),
+    W.custom("fp8_wider_64", T=192, H=256, I=256, E=32, k=4, dtype=W.FP8, seed=49,
+             logits="nan_rows"),
 ]
 
 
