@@ -39,6 +39,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
+#include <mutex>
+
 #include "gemm_common.cuh"
 #include "moe_internal.cuh"
 #include "ptx.cuh"
@@ -645,11 +647,21 @@ template <int KIND, int NT, int MODE>
 static cudaError_t launch_mode(const GemmArgs& args, const GemmMaps* maps, int grid, int smem,
                                cudaStream_t stream) {
   auto kern = moe_gemm_kernel<KIND, NT, MODE>;
-  static int configured = 0;  // max dynamic smem is a per-function attribute
-  if (configured < smem) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // max dynamic smem is a per-function attribute, raised once per size (and
+  // again after a switch of device); host threads may launch concurrently
+  static std::mutex mu;
+  static int configured = 0, conf_dev = -1;
+  {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    configured = smem;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev != conf_dev || configured < smem) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      configured = dev != conf_dev ? smem : (configured > smem ? configured : smem);
+      conf_dev = dev;
+    }
   }
   return launch_chained(kern, dim3(grid), dim3(kThreads), static_cast<size_t>(smem), stream,
                         maps[0], maps[1], args);

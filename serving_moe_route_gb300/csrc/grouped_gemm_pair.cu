@@ -28,6 +28,8 @@
 // Both CTAs walk the same item sequence (items c, c + clusters, ...).  Every
 // wait is bounded; a CTA that gives up raises the timeout bit and both CTAs
 // meet at the final cluster barrier before TMEM is freed.
+#include <mutex>
+
 #include "gemm_common.cuh"
 
 namespace moe {
@@ -365,12 +367,20 @@ template <int KIND, int MODE>
 static cudaError_t launch_pair_mode(const GemmArgs& args, const GemmMaps& maps, int smem,
                                     long long max_items, cudaStream_t stream) {
   auto kern = moe_gemm_pair_kernel<KIND, MODE>;
-  static int configured = 0;  // max dynamic smem is a per-function attribute
-  static int clusters = 0;    // co-resident clusters at that smem size
-  if (configured < smem) {
+  // max dynamic smem (a per-function attribute) and the co-resident cluster
+  // count at that size, set up once per size and device; host threads may
+  // launch concurrently
+  static std::mutex mu;
+  static int configured = 0, conf_dev = -1, clusters = 0;
+  int dev = 0;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return de;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev != conf_dev || configured != smem) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     configured = smem;
+    conf_dev = dev;
     clusters = 0;
   }
   if (clusters == 0) {
