@@ -32,7 +32,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "fused-MoE layer µs/call & tokens/s vs batch; % of HBM/tensor roofline, 1 GB300"
-HBM_NORTH_STAR_GBS = 8000.0
+HBM_ROOFLINE_GBS = 8000.0
 FLUSH_BYTES = 256 << 20
 SWEEP = ["decode_bf16", "decode_grouped_bf16", "sparse_uniform_bf16", "sparse_concentrated_bf16",
          "sparse_uniform_bf16_old_est", "sparse_concentrated_bf16_old_est",
@@ -397,7 +397,7 @@ def layer_roofline(wl, step_ms, acc, pk):
     if wl.dtype == W.F32:
         tp = pk["bf16_tflops"] / 2.0
     t_c = acc["flops"] / (tp * 1e12)
-    t_ns = max(t_c, acc["layer_bytes"] / (HBM_NORTH_STAR_GBS * 1e9))
+    t_ns = max(t_c, acc["layer_bytes"] / (HBM_ROOFLINE_GBS * 1e9))
     t_meas = max(t_c, acc["layer_bytes"] / (pk["hbm_gbs"] * 1e9))
     s = step_ms * 1e-3
     return {"floor_us_8tbs": round(t_ns * 1e6, 2), "frac_8tbs": round(t_ns / s, 4),
