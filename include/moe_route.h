@@ -5,9 +5,9 @@
  *   a-1  NaN-safe softmax / sigmoid top-k routing with k distinct ids
  *        (PR #39593 "Fix FlashInfer CUTLASS BF16 + CUDA graphs IMA",
  *        section "Fix": NaN replaced by -FLT_MAX in-register before scoring
- *        and before the arg-max; "topK now returns K distinct indices"),
- *   a-2  count and permute token rows by expert (H20 article, para. 3:
- *        "the number of rows assigned to each expert"),
+ *        and before the arg-max, so that top-k yields k distinct ids),
+ *   a-2  count and permute token rows by expert (H20 article, para. 3: the
+ *        rows each expert receives),
  *   a-3  the tile plan from the rows-per-expert estimate
  *        est = max(1, ceil(T*k/E)), applied after the worst-case workspace
  *        capacity is fixed (H20 article, para. 3),
