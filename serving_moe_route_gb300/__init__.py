@@ -6,7 +6,8 @@ and the top-k weighted combine fused into their epilogues, behind the C ABI
 in ``include/moe_route.h``.
 """
 from ._binding import MoeError, MoePlan, lib, moe_plan  # noqa: F401
+from .ep import ep_forward  # noqa: F401
 from .layer import BF16, F32, FP8, SIGMOID, SOFTMAX, MoELayer, route_topk  # noqa: F401
 
-__all__ = ["MoELayer", "MoePlan", "MoeError", "route_topk", "moe_plan", "lib", "F32", "BF16",
-           "FP8", "SOFTMAX", "SIGMOID"]
+__all__ = ["MoELayer", "MoePlan", "MoeError", "route_topk", "ep_forward", "moe_plan", "lib",
+           "F32", "BF16", "FP8", "SOFTMAX", "SIGMOID"]
