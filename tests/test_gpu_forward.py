@@ -243,3 +243,35 @@ def test_expert_parallel_slices(dtype):
     tol = PU.TOL[dtype] * np.abs(full_out).max()
     assert np.abs(total - full_out).max() <= tol
 
+
+
+@pytest.mark.gpu
+def test_ep_forward_single_rank_nccl():
+    # the expert-parallel exchange driving the GPU layer through NCCL; with
+    # one rank every pick is local, so it must reproduce the plain layer
+    import socket
+
+    import torch.distributed as dist
+
+    from serving_moe_route_gb300 import route_topk
+    from serving_moe_route_gb300.ep import ep_forward
+
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        port = s.getsockname()[1]
+    dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0, world_size=1)
+    try:
+        wl = W.custom("ep_nccl", T=40, H=256, I=128, E=16, k=4, dtype=W.BF16, seed=62,
+                      logits="nan_rows")
+        inp = W.make_inputs(wl)
+        layer = PU.make_layer(wl, inp)
+        dev = layer.device
+        x, lg = inp["x"].to(dev), inp["logits"].to(dev)
+        got = ep_forward(x, lg, k=wl.k, E=wl.E, route=lambda t: route_topk(t, wl.k),
+                         local_forward=layer.forward_with_ids)
+        torch.cuda.synchronize()
+        tokens = np.arange(wl.T, dtype=np.int32)
+        ref, _, _ = PU.run_oracle(wl, inp, tokens)
+        PU.check_outputs(wl, got.double().cpu().numpy(), ref, tokens)
+    finally:
+        dist.destroy_process_group()
