@@ -2,13 +2,20 @@
 """Benchmark of the fused MoE layer forward on one GB300 (per rank).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--sweep]
+                    [--workload NAME] [--no-sweep]
 
 A step is one call of the whole layer (routing, permutation, grouped gate+up
 GEMM with SiLU, grouped down GEMM with the weighted combine, output cast)
 over one batch whose inputs are already resident in HBM.  Between timed
 steps a 256 MiB buffer is written to flush L2, outside the per-step CUDA
 events.  Rank 0 prints one JSON line.
+
+After the headline's timed region, rank 0 also measures the batch sweep of
+the metric: every workload (decode, sparse E=400 with and without the old
+estimate and the EP8 slice, the FP8 batch sweep T=1..4096, skewed prefill)
+timed as µs per call over 24 CUDA-graph replays after 5 warm-ups, each with
+its roofline fractions, plus the routing micro-benchmark (--no-sweep skips
+both).
 
 Under torchrun every rank runs an independent replica of the layer on its
 own GPU (tokens are independent; there is no exchange step), so the work
@@ -48,10 +55,9 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="decode_bf16")
-    ap.add_argument("--sweep", action="store_true", help="also time every workload (rank 0)")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the per-workload sweep and the routing micro-benchmark")
     ap.add_argument("--sweep-samples", type=int, default=24)
-    ap.add_argument("--routing", action="store_true",
-                    help="also run the routing micro-benchmark (rank 0)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -119,6 +125,51 @@ def peaks():
                 "source": "measured"}
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
             "source": "fallback"}
+
+
+def measure_fp8_peak(dev, n=8192, reps=10):
+    """Dense FP8 (e4m3 x e4m3 -> bf16) matmul throughput of this GPU: the
+    best of `reps` CUDA-event-timed torch._scaled_mm calls on n x n x n
+    (2 n^3 FLOP each), after three warm-up calls.  Returns TFLOP/s, or None
+    when the call is unavailable."""
+    import torch
+    try:
+        g = torch.Generator(device="cpu")
+        g.manual_seed(8)
+        a = torch.randn(n, n, generator=g).to(dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, generator=g).to(dev).to(torch.float8_e4m3fn)
+        one = torch.ones((), dtype=torch.float32, device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize(dev)
+        best = None
+        for _ in range(reps):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch._scaled_mm(a, b.t(), scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            ms = e0.elapsed_time(e1)
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return round(2.0 * n ** 3 / (best * 1e-3) / 1e12, 1)
+    except (RuntimeError, AttributeError, TypeError):
+        return None
+
+
+def tensor_peak(wl, pk):
+    """Dense tensor peak (TFLOP/s) for the workload's operand type: bf16
+    measured; FP8 measured by the probe when it ran, else 2 x bf16 (the
+    nominal ratio); TF32 half of bf16 (nominal ratio)."""
+    from serving_moe_route_gb300 import workloads as W
+    if wl.dtype == W.FP8:
+        if pk.get("fp8_tflops"):
+            return pk["fp8_tflops"], "measured (torch._scaled_mm e4m3 8192^3 probe)"
+        return 2.0 * pk["bf16_tflops"], "2 x measured bf16 (nominal ratio; fp8 probe unavailable)"
+    if wl.dtype == W.F32:
+        return pk["bf16_tflops"] / 2.0, "measured bf16 / 2 (nominal tf32 ratio)"
+    return pk["bf16_tflops"], pk["source"]
 
 
 # ------------------------------------------------------------ accounting
@@ -370,10 +421,8 @@ def gemm_roofline(wl, stage_ms, acc, pk):
     else:
         name, ms, nbytes, flops = "gemm2", g2, acc["g2_bytes"], acc["flops"] / 3.0
     t_mem = nbytes / (pk["hbm_gbs"] * 1e9)
-    tensor_peak = pk["bf16_tflops"] * (2.0 if wl.dtype == W.FP8 else 1.0)
-    if wl.dtype == W.F32:
-        tensor_peak = pk["bf16_tflops"] / 2.0
-    t_cmp = flops / (tensor_peak * 1e12)
+    tensor_pk, tensor_src = tensor_peak(wl, pk)
+    t_cmp = flops / (tensor_pk * 1e12)
     if t_mem >= t_cmp:
         achieved = nbytes / (ms * 1e-3) / 1e9
         return name, {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
@@ -382,20 +431,16 @@ def gemm_roofline(wl, stage_ms, acc, pk):
                       "algorithmic_bytes": int(nbytes), "mean_ms": round(ms, 5),
                       "peak_source": pk["source"]}
     achieved = flops / (ms * 1e-3) / 1e12
-    return name, {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_peak,
-                  "unit": "TFLOP/s", "frac": round(achieved / tensor_peak, 4), "traffic": None,
+    return name, {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_pk,
+                  "unit": "TFLOP/s", "frac": round(achieved / tensor_pk, 4), "traffic": None,
                   "kernel": f"moe_gemm_kernel ({name})", "algorithmic_flops": flops,
-                  "mean_ms": round(ms, 5), "peak_source": pk["source"] + (
-                      " (fp8 = 2x bf16 nominal ratio)" if wl.dtype == W.FP8 else "")}
+                  "mean_ms": round(ms, 5), "peak_source": tensor_src}
 
 
 def layer_roofline(wl, step_ms, acc, pk):
     """North-star roofline of the whole layer: max(FLOPs / tensor peak,
     bytes / 8 TB/s); also against the measured copy bandwidth."""
-    from serving_moe_route_gb300 import workloads as W
-    tp = pk["bf16_tflops"] * (2.0 if wl.dtype == W.FP8 else 1.0)
-    if wl.dtype == W.F32:
-        tp = pk["bf16_tflops"] / 2.0
+    tp, _ = tensor_peak(wl, pk)
     t_c = acc["flops"] / (tp * 1e12)
     t_ns = max(t_c, acc["layer_bytes"] / (HBM_ROOFLINE_GBS * 1e9))
     t_meas = max(t_c, acc["layer_bytes"] / (pk["hbm_gbs"] * 1e9))
@@ -406,35 +451,61 @@ def layer_roofline(wl, step_ms, acc, pk):
             "flops": acc["flops"], "bytes": acc["layer_bytes"], "touched_experts": acc["touched"]}
 
 
-def cpu_baseline(wl, inp, seconds):
-    """The oracle as it stands, on the host cores, on the first n tokens of
-    the same workload (n sized to about `seconds` of work)."""
-    import numpy as np
-
-    import oracle
+def oracle_args(wl, inp):
     from serving_moe_route_gb300 import workloads as W
-    cores = len(os.sched_getaffinity(0))
-    oracle.set_threads(cores)
-    args = dict(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, dtype=wl.dtype, scoring=wl.scoring,
+    return dict(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, dtype=wl.dtype, scoring=wl.scoring,
                 renorm=wl.renorm, x=W.storage_numpy(inp["x"]),
                 logits=W.storage_numpy(inp["logits"]), w13=W.storage_numpy(inp["w13"]),
                 w2=W.storage_numpy(inp["w2"]), s13=W.storage_numpy(inp["s13"]),
                 s2=W.storage_numpy(inp["s2"]), ep_size=wl.ep_size, ep_rank=wl.ep_rank,
                 n_group=wl.n_group, topk_group=wl.topk_group)
+
+
+def time_oracle(args, n_tokens, seconds):
+    """Passes of the oracle over the first n_tokens tokens until about
+    `seconds` have gone by (at least one).  Returns (tokens/s, passes, s)."""
+    import numpy as np
+
+    import oracle
+    toks = np.arange(n_tokens, dtype=np.int32)
+    t0 = time.perf_counter()
+    passes = 0
+    while True:
+        oracle.moe_forward(**args, tokens=toks)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= seconds:
+            return n_tokens * passes / dt, passes, dt
+
+
+def cpu_baseline(wl, inp, seconds):
+    """The oracle as it stands, on the host cores: OpenMP over tokens on
+    every core, passes over a token sample for about `seconds`; for batches
+    of at most 128 tokens also one thread on a smaller sample."""
+    import numpy as np
+
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    oracle.set_threads(cores)
+    args = oracle_args(wl, inp)
     n = min(wl.T, max(1, cores))
     t0 = time.perf_counter()
     oracle.moe_forward(**args, tokens=np.arange(n, dtype=np.int32))
-    dt = time.perf_counter() - t0
-    n2 = int(min(wl.T, max(n, n * seconds / max(dt, 1e-6))))
-    if n2 > n:
-        t0 = time.perf_counter()
-        oracle.moe_forward(**args, tokens=np.arange(n2, dtype=np.int32))
-        dt = time.perf_counter() - t0
-        n = n2
-    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": oracle.threads(),
-            "kind": "oracle",
-            "sample": f"first {n} of {wl.T} tokens of {wl.name} (routing, expert MLPs and combine "
-                      f"for those tokens), {dt:.2f} s, OpenMP over tokens"}
+    dt = max(time.perf_counter() - t0, 1e-6)
+    n = int(min(wl.T, max(n, n * seconds / dt)))  # one pass of about `seconds` at most
+    rate, passes, dt = time_oracle(args, n, seconds)
+    out = {"value": round(rate, 3), "unit": "tokens/s", "cores": oracle.threads(),
+           "kind": "oracle",
+           "sample": f"first {n} of {wl.T} tokens of {wl.name} (routing, expert MLPs and combine "
+                     f"for those tokens) x {passes} passes, {dt:.2f} s, OpenMP over tokens"}
+    if wl.T <= 128:
+        oracle.set_threads(1)
+        n1 = min(wl.T, 16)
+        r1, p1, d1 = time_oracle(args, n1, seconds / 4)
+        out["single_thread"] = {"value": round(r1, 3), "unit": "tokens/s", "cores": 1,
+                                "sample": f"first {n1} tokens x {p1} passes, {d1:.2f} s"}
+        oracle.set_threads(cores)
+    return out
 
 
 def routing_bench(dev, calls=500):
@@ -527,6 +598,20 @@ def sweep(dev, samples, pk):
     return rows
 
 
+def estimate_ablation(rows):
+    """The H20 article's comparison on each workload that the sweep also ran
+    with the old token-count estimate: µs per call of each, and old / new
+    (above 1: the rows-per-expert estimate is faster)."""
+    us = {r["workload"]: r["us_median"] for r in rows}
+    out = {}
+    for name, new in us.items():
+        old = us.get(name + "_old_est")
+        if old:
+            out[name] = {"us_estimate": new, "us_old_estimate": old,
+                         "old_over_new": round(old / new, 3)}
+    return out
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -607,11 +692,22 @@ def run_ours(args):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, inp, args.cpu_seconds)
-    if rank == 0 and (args.sweep or args.routing):
-        line["routing_microbench"] = routing_bench(dev)
-    if rank == 0 and args.sweep:
+    if rank == 0 and not args.no_sweep:
+        # the batch sweep of the metric (every workload, 24 samples after 5
+        # warm-ups each) and the routing micro-benchmark, after the headline's
+        # timed region; FP8 rooflines divide by the measured FP8 peak
         del r
+        pk["fp8_tflops"] = measure_fp8_peak(dev)
+        line["peaks"] = {"hbm_gbs": pk["hbm_gbs"], "bf16_tflops": pk["bf16_tflops"],
+                         "fp8_tflops": pk["fp8_tflops"],
+                         "fp8_source": "torch._scaled_mm e4m3 8192^3, best of 10 (this run)"
+                         if pk["fp8_tflops"] else "unavailable: 2 x bf16 used",
+                         "source": pk["source"]}
+        line["routing_microbench"] = routing_bench(dev)
+        t0 = time.perf_counter()
         line["sweep"] = sweep(dev, args.sweep_samples, pk)
+        line["sweep_wall_s"] = round(time.perf_counter() - t0, 1)
+        line["estimate_ablation"] = estimate_ablation(line["sweep"])
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -633,12 +729,7 @@ def run_reference(args):
     inp = W.make_inputs(wl)
     cores = len(os.sched_getaffinity(0))
     oracle.set_threads(cores)
-    fa = dict(T=wl.T, H=wl.H, I=wl.I, E=wl.E, k=wl.k, dtype=wl.dtype, scoring=wl.scoring,
-              renorm=wl.renorm, x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
-              w13=W.storage_numpy(inp["w13"]), w2=W.storage_numpy(inp["w2"]),
-              s13=W.storage_numpy(inp["s13"]), s2=W.storage_numpy(inp["s2"]),
-              ep_size=wl.ep_size, ep_rank=wl.ep_rank, n_group=wl.n_group,
-              topk_group=wl.topk_group)
+    fa = oracle_args(wl, inp)
     n = min(wl.T, max(1, cores))  # tokens per step: one per host core
     toks = np.arange(n, dtype=np.int32)
     for _ in range(max(0, args.warmup)):

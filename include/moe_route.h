@@ -19,7 +19,10 @@
  * Conventions for every call:
  *  - Every pointer argument named "device" is a device pointer the caller
  *    owns (e.g. from torch); the library never allocates device memory and
- *    keeps no state beyond a per-device cache of kernel attributes.
+ *    keeps no state beyond a per-device cache of kernel attributes and a
+ *    cache of TMA tensor maps keyed by device, pointers and shapes (a map
+ *    encodes only an address, a shape and a box, so an entry stays valid
+ *    while the same pointers come with the same shapes).
  *  - `stream` is a cudaStream_t passed as void*; all device work is
  *    enqueued on it asynchronously.  No call below synchronises, except
  *    moe_check.
@@ -284,16 +287,29 @@ int moe_plan_describe(const moe_plan_t* plan, char* buf, size_t n);
  * layouts, alignment and errors as moe_forward.
  *
  * The first call on each device looks up the array's device address
- * (a synchronous runtime query); make that first call before any stream
- * capture.  Every call on a device uses the same array and leaves its
- * contents behind; the call clears what must start at zero itself.  Calls
- * whose work overlaps on the GPU (other streams, other threads) race on the
- * array: serialise them.  The device error word lives in that array, so
- * moe_check is not available for this entry point.
+ * (a synchronous runtime query, with that device current); make that first
+ * call before any stream capture.  The address is looked up again when the
+ * device's context changes (after cudaDeviceReset, for example), and that
+ * next call is again a first call.  Every call on a device uses the same
+ * array and leaves its contents behind; the call clears what must start at
+ * zero itself.  Calls whose work overlaps on the GPU (other streams, other
+ * threads) race on the array: serialise them.  The device error word lives
+ * in that array; read it with moe_check_noalloc.
  */
 int moe_forward_noalloc(const moe_plan_t* plan, const void* x, const void* logits,
                         const void* w13, const float* s13, const void* w2, const float* s2,
                         void* out, void* stream);
+
+/*
+ * moe_check_noalloc -- moe_check for moe_forward_noalloc: synchronise
+ * `stream`, read and clear the error word in the built-in workspace of the
+ * current device (at plan->off_err), and return MOE_OK, MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE as moe_check does; *bits (if not NULL) receives the word.
+ * Allocates nothing.  MOE_ERR_WORKSPACE for a plan too large for the
+ * built-in workspace; MOE_ERR_INVALID_ARG for a bad plan.  The pages have no
+ * counterpart of this call either.
+ */
+int moe_check_noalloc(const moe_plan_t* plan, uint32_t* bits, void* stream);
 
 /* moe_strerror -- static message for a MOE_* return code. */
 const char* moe_strerror(int code);

@@ -28,7 +28,7 @@ MOE_LOGITS_F32, MOE_LOGITS_BF16 = 0, 1
 MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 
 EXPORTED = ("moe_plan", "moe_plan_ep", "moe_forward", "moe_forward_timed", "moe_forward_with_ids",
-            "moe_forward_noalloc", "moe_route_topk", "moe_route_grouped_topk",
+            "moe_forward_noalloc", "moe_check_noalloc", "moe_route_topk", "moe_route_grouped_topk",
             "moe_plan_set_groups", "moe_check", "moe_plan_describe",
             "moe_strerror", "moe_abi_version")
 
@@ -98,6 +98,8 @@ def lib() -> ctypes.CDLL:
     L.moe_forward_with_ids.restype = i
     L.moe_forward_noalloc.argtypes = [ctypes.POINTER(MoePlan), P, P, P, P, P, P, P, P]
     L.moe_forward_noalloc.restype = i
+    L.moe_check_noalloc.argtypes = [ctypes.POINTER(MoePlan), ctypes.POINTER(c_u32), P]
+    L.moe_check_noalloc.restype = i
     L.moe_route_topk.argtypes = [P, i, i, i, i, i, i, P, P, P]
     L.moe_route_grouped_topk.argtypes = [P, i, i, i, i, i, i, i, i, P, P, P]
     L.moe_route_grouped_topk.restype = i
@@ -162,6 +164,13 @@ def moe_forward_noalloc(plan, x, logits, w13, s13, w2, s2, out, stream):
     """moe_forward with the library's built-in 16 MiB device workspace (no
     allocation anywhere); for callers that cannot allocate device memory."""
     return lib().moe_forward_noalloc(ctypes.byref(plan), x, logits, w13, s13, w2, s2, out, stream)
+
+
+def moe_check_noalloc(plan, stream):
+    """(rc, error bits) of the built-in workspace after moe_forward_noalloc."""
+    bits = c_u32(0)
+    rc = lib().moe_check_noalloc(ctypes.byref(plan), ctypes.byref(bits), stream)
+    return rc, bits.value
 
 
 def moe_route_topk(logits, logits_dtype, T, E, k, scoring, renorm, ids, w, stream):

@@ -15,8 +15,10 @@
 //                   a tile list, else one launch each
 //   combine_kernel  a-7: out[t] = sum over j of the token's k weighted rows,
 //                   in pick order (fp32 sum, deterministic)
-// No atomics are used to count or place rows: every slot follows from
-// counts and ranks computed without them.
+// No atomics are used to count or place rows: a pick's rank is the number of
+// equal ids before it in its routing CTA, the CTA's count of an expert is
+// written once (by that expert's last pick there, as rank + 1), the scan
+// adds the CTAs' counts in CTA order, and every slot follows from those.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -209,7 +211,9 @@ __global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
   __syncthreads();
 
   // each pick's rank among the equal ids before it (a warp per pick, its
-  // lanes splitting the earlier picks), and this CTA's per-expert counts
+  // lanes splitting the CTA's picks), and this CTA's per-expert counts: the
+  // last pick of an expert in the CTA (no equal id after it) is its only
+  // writer, and stores rank + 1
   const int n = ntok * k;
   int* cnt = sid + tpc * k;
   for (int e = threadIdx.x; e < e_local; e += blockDim.x) cnt[e] = 0;
@@ -217,11 +221,17 @@ __global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
   for (int f = warp; f < n; f += nwarps) {
     const int e = sid[f];
     int r = 0;
-    for (int g = lane; g < f; g += 32) r += (sid[g] == e);
+    bool later = false;
+    for (int g = lane; g < n; g += 32) {
+      const bool same = sid[g] == e;
+      r += (g < f && same);
+      later |= (g > f && same);
+    }
     r = __reduce_add_sync(0xffffffffu, r);
+    later = __any_sync(0xffffffffu, later);
     if (lane == 0) {
       lrank[static_cast<size_t>(t0) * k + f] = (e >= 0) ? r : -1;
-      if (e >= 0) atomicAdd(&cnt[e], 1);  // order-free: the count is exact
+      if (e >= 0 && !later) cnt[e] = r + 1;
     }
   }
   __syncthreads();
@@ -580,6 +590,88 @@ static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The TMA tensor maps of one forward: weights (w13, w2) and the permuted
+// token rows (xq, act) at every box height, plus the half-height token maps
+// of CTA-pair plans.  A map only encodes an address, a shape and a box, so
+// an entry stays valid for as long as the caller passes the same pointers
+// with the same shapes (also when a buffer is freed and another of the same
+// shape is allocated at the same address).
+struct MapKey {
+  int dev, kind, H, I, EL, pair;
+  long long R;
+  const void *w13, *w2, *xq, *act;
+  bool operator==(const MapKey& o) const {
+    return dev == o.dev && kind == o.kind && H == o.H && I == o.I && EL == o.EL &&
+           pair == o.pair && R == o.R && w13 == o.w13 && w2 == o.w2 && xq == o.xq &&
+           act == o.act;
+  }
+};
+struct MapSet {
+  GemmMaps m1, m2, h1, h2;  // h1/h2: half-height token maps (CTA pairs)
+};
+
+static bool encode_maps(const MapKey& key, MapSet* s) {
+  const int esize = key.kind == KIND_TF32 ? 4 : key.kind == KIND_BF16 ? 2 : 1;
+  const CUtensorMapDataType dt = key.kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : key.kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                         : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  bool ok = make_tmap(&s->m1.a, key.w13, dt, esize, key.H, static_cast<uint64_t>(key.EL) * 2 * key.I,
+                      128) &&
+            make_tmap(&s->m2.a, key.w2, dt, esize, key.I, static_cast<uint64_t>(key.EL) * key.H,
+                      128);
+  for (int i = 0; i < kTokMaps && ok; ++i) {  // token boxes 16 .. 256 rows
+    const uint32_t rows = 16u << i;
+    ok = make_tmap(&s->m1.b[i], key.xq, dt, esize, key.H, key.R, rows) &&
+         make_tmap(&s->m2.b[i], key.act, dt, esize, key.I, key.R, rows);
+  }
+  s->h1 = s->m1;
+  s->h2 = s->m2;
+  for (int i = 0; i < kTokMaps && ok && key.pair; ++i) {  // half tiles 8 .. 128 rows
+    const uint32_t rows = 8u << i;
+    ok = make_tmap(&s->h1.b[i], key.xq, dt, esize, key.H, key.R, rows) &&
+         make_tmap(&s->h2.b[i], key.act, dt, esize, key.I, key.R, rows);
+  }
+  return ok;
+}
+
+// A small cache of encoded map sets, most recently used first; host threads
+// may call concurrently.  The copy out is taken under the lock.
+static bool cached_maps(const MapKey& key, MapSet* out) {
+  constexpr int kEntries = 16;
+  static MapKey keys[kEntries];
+  static MapSet sets[kEntries];
+  static int used = 0;
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < used; ++i) {
+    if (keys[i] == key) {
+      *out = sets[i];
+      if (i > 0) {  // move to the front
+        const MapKey kk = keys[i];
+        const MapSet ss = sets[i];
+        for (int j = i; j > 0; --j) {
+          keys[j] = keys[j - 1];
+          sets[j] = sets[j - 1];
+        }
+        keys[0] = kk;
+        sets[0] = ss;
+      }
+      return true;
+    }
+  }
+  MapSet s;
+  if (!encode_maps(key, &s)) return false;
+  if (used < kEntries) ++used;
+  for (int j = used - 1; j > 0; --j) {  // the least recently used entry drops out
+    keys[j] = keys[j - 1];
+    sets[j] = sets[j - 1];
+  }
+  keys[0] = key;
+  sets[0] = s;
+  *out = s;
+  return true;
+}
+
 static int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -692,12 +784,12 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   // double-buffered tile; GEMM2 (one accumulator) widens hot experts to 256
   // tokens in prefill-sized plans (est > 64).  CTA pairs: 256 for both
   // (each CTA holds half of the tile's rows).
-  const bool pair = p->gemm_pair != 0 && !fp8;
-  const int NM1 = pair ? 256 : fp8 ? fp8_nt : 128;
-  const int NM2 = pair ? 256 : fp8 ? fp8_nt : (p->tile_n >= 128 ? 256 : 128);
+  const bool pair_plan = p->gemm_pair != 0 && !fp8;
+  const int NM1 = pair_plan ? 256 : fp8 ? fp8_nt : 128;
+  const int NM2 = pair_plan ? 256 : fp8 ? fp8_nt : (p->tile_n >= 128 ? 256 : 128);
   launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, p->tile_n,
                  per_expert, NM1, NM2, p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
-                 tiles2, ntiles2, dep, pair ? 1 : 0, err);
+                 tiles2, ntiles2, dep, pair_plan ? 1 : 0, err);
   mark(2);
   // a-2 gather
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
@@ -718,18 +810,14 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const int kind = p->dtype == MOE_DTYPE_F32 ? KIND_TF32
                    : p->dtype == MOE_DTYPE_BF16 ? KIND_BF16 : KIND_E4M3;
   const int esize = kind == KIND_TF32 ? 4 : kind == KIND_BF16 ? 2 : 1;
-  const CUtensorMapDataType dt = kind == KIND_TF32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                 : kind == KIND_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
-                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  GemmMaps m1, m2;
-  bool maps_ok = make_tmap(&m1.a, w13, dt, esize, H, static_cast<uint64_t>(EL) * 2 * I, 128) &&
-                 make_tmap(&m2.a, w2, dt, esize, I, static_cast<uint64_t>(EL) * H, 128);
-  for (int i = 0; i < kTokMaps && maps_ok; ++i) {  // token boxes 16 .. 256 rows
-    const uint32_t rows = 16u << i;
-    maps_ok = make_tmap(&m1.b[i], xq, dt, esize, H, R, rows) &&
-              make_tmap(&m2.b[i], act, dt, esize, I, R, rows);
-  }
-  if (!maps_ok) return MOE_ERR_CUDA;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool pair = pair_plan;
+  MapSet ms;
+  if (!cached_maps(MapKey{dev, kind, H, I, EL, pair ? 1 : 0, R, w13, w2, xq, act}, &ms))
+    return MOE_ERR_CUDA;
+  const GemmMaps& m1 = ms.m1;
+  const GemmMaps& m2 = ms.m2;
 
   const int sms = sm_count();
   if (sms <= 0) return MOE_ERR_CUDA;
@@ -738,13 +826,8 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   if (pair) {
     // CTA pairs: half-height token maps, items of 256 weight rows, one
     // token tile list (widths up to 256) for both GEMMs
-    GemmMaps h1 = m1, h2 = m2;
-    for (int i = 0; i < kTokMaps && maps_ok; ++i) {
-      const uint32_t rows = 8u << i;
-      maps_ok = make_tmap(&h1.b[i], xq, dt, esize, H, R, rows) &&
-                make_tmap(&h2.b[i], act, dt, esize, I, R, rows);
-    }
-    if (!maps_ok) return MOE_ERR_CUDA;
+    const GemmMaps& h1 = ms.h1;
+    const GemmMaps& h2 = ms.h2;
     GemmArgs g{};
     g.p[0] = GemmPhase{tiles, ntiles, 2, 256, (I + 255) / 256, kb1, 2 * I, I, I, nullptr, 0,
                        nullptr};
@@ -1073,19 +1156,48 @@ int moe_check(const moe_plan_t* plan, void* ws, uint32_t* bits, void* stream) {
 static constexpr size_t kNoAllocWorkspaceBytes = size_t(16) << 20;  // 16 MiB
 static __device__ __align__(256) unsigned char g_noalloc_workspace[kNoAllocWorkspaceBytes];
 
-// Device address of g_noalloc_workspace, looked up once per device.  In host
-// code the array's name is only a host-side stand-in, never a device
-// address, so it must not be passed to a kernel.
-static void* noalloc_workspace_ptr(int dev) {
+// The calling thread's current CUDA context (driver API, looked up through
+// the runtime's entry-point query), or null.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+static CUcontext current_context() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
+
+// Device address of g_noalloc_workspace, looked up with that device current
+// the first time a device (and context) calls.  In host code the array's
+// name is only a host-side stand-in, never a device address, so it must not
+// be passed to a kernel.  The address is remembered together with the
+// context it was looked up in: after cudaDeviceReset, or when the primary
+// context is torn down and created again, the module is loaded anew and the
+// address is looked up again on the next call.
+static void* noalloc_workspace_ptr() {
   constexpr int kMaxDevices = 64;
   static void* ptrs[kMaxDevices] = {};
+  static CUcontext ctxs[kMaxDevices] = {};
   static std::mutex mu;
-  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  const CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
+  if (!ptrs[dev] || !ctx || ctxs[dev] != ctx) {
+    // no context bound to this thread yet, a new device, or a new context:
+    // the runtime query binds the device's context and loads the module
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess) return nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || !p) return nullptr;
     ptrs[dev] = p;
+    ctxs[dev] = current_context();
   }
   return ptrs[dev];
 }
@@ -1095,14 +1207,20 @@ int moe_forward_noalloc(const moe_plan_t* plan, const void* x, const void* logit
                         void* out, void* stream) {
   if (!plan_ok(plan)) return MOE_ERR_INVALID_ARG;
   if (plan->workspace_bytes > kNoAllocWorkspaceBytes) return MOE_ERR_WORKSPACE;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  void* ws = noalloc_workspace_ptr(dev);
+  void* ws = noalloc_workspace_ptr();
   if (!ws) return MOE_ERR_CUDA;
   // the error word is the only region that must start from zero; the
   // forward clears it on the stream before its first kernel
   return forward_impl(plan, x, logits, nullptr, nullptr, w13, s13, w2, s2, out, ws,
                       kNoAllocWorkspaceBytes, stream);
+}
+
+int moe_check_noalloc(const moe_plan_t* plan, uint32_t* bits, void* stream) {
+  if (!plan_ok(plan)) return MOE_ERR_INVALID_ARG;
+  if (plan->workspace_bytes > kNoAllocWorkspaceBytes) return MOE_ERR_WORKSPACE;
+  void* ws = noalloc_workspace_ptr();
+  if (!ws) return MOE_ERR_CUDA;
+  return moe_check(plan, ws, bits, stream);
 }
 
 }  // extern "C"

@@ -44,3 +44,30 @@ def test_algorithmic_accounting_decode():
     assert acc["touched"] == 128
     # layer bytes: touched weights + logits + x + out
     assert acc["layer_bytes"] == 128 * (6291456 + 3145728) + 128 * 128 * 2 + 2 * 128 * 2048 * 2
+
+
+def test_tensor_peak_per_operand_type():
+    pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "measured"}
+    wls = W.workloads()
+    assert bench.tensor_peak(wls["decode_bf16"], pk)[0] == 1900.0
+    assert bench.tensor_peak(wls["tiny_f32"], pk)[0] == 950.0
+    # FP8 without a probe: the nominal 2x ratio, and it says so
+    v, src = bench.tensor_peak(wls["fp8_T16"], pk)
+    assert v == 3800.0 and "nominal" in src
+    pk["fp8_tflops"] = 3500.0
+    v, src = bench.tensor_peak(wls["fp8_T16"], pk)
+    assert v == 3500.0 and "measured" in src
+
+
+def test_estimate_ablation_pairs_old_and_new():
+    rows = [{"workload": "a", "us_median": 50.0}, {"workload": "a_old_est", "us_median": 100.0},
+            {"workload": "b", "us_median": 10.0}]
+    ab = bench.estimate_ablation(rows)
+    assert list(ab) == ["a"] and ab["a"]["old_over_new"] == 2.0
+
+
+def test_every_benchmarked_workload_is_a_named_workload():
+    # the GPU parity suite runs every named workload on all of its tokens,
+    # so nothing the sweep times goes without a parity test
+    assert set(bench.SWEEP) <= set(W.workloads())
+    assert "decode_bf16" in bench.SWEEP

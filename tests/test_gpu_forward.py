@@ -1,7 +1,7 @@
 """GPU parity of the whole layer (moe_forward through the C ABI) against the
-oracle on the workloads of the pages and on edge cases: routing and
-permutation bit-exact on every token, outputs within tolerance on all
-tokens (small cases) or on a sampled set of tokens (full-size cases)."""
+oracle on every named workload (all that the benchmark times) and on edge
+cases: routing and permutation bit-exact on every token, outputs within
+tolerance on every token."""
 import numpy as np
 import pytest
 import torch
@@ -16,21 +16,16 @@ pytestmark = pytest.mark.gpu
 
 WL = W.workloads()
 
-FULL = ["tiny_f32", "decode_bf16", "decode_grouped_bf16", "sparse_uniform_bf16",
-        "sparse_concentrated_bf16", "sparse_uniform_bf16_ep8",
-        "sparse_uniform_bf16_old_est", "fp8_T1", "fp8_T2", "fp8_T16", "fp8_T64", "fp8_T128",
-        "fp8_T256", "fp8_T1024", "fp8_T4096", "skewed_prefill_bf16", "skewed_prefill_sigmoid_bf16"]
 
-
-@pytest.mark.parametrize("name", FULL)
+@pytest.mark.parametrize("name", list(WL))
 def test_forward_workload(name):
     wl = WL[name]
     inp = PU.inputs(wl)
     out, inter, _ = PU.run_gpu(wl, inp)
     PU.check_routing_and_permutation(wl, inp, inter)
-    tokens = PU.sample_tokens(wl, inp, n=48 if wl.T > 1024 else 64)
+    tokens = PU.all_tokens(wl)
     ref, ids_o, _ = PU.run_oracle(wl, inp, tokens)
-    np.testing.assert_array_equal(inter["ids"][tokens], ids_o)
+    np.testing.assert_array_equal(inter["ids"], ids_o)
     PU.check_outputs(wl, out, ref, tokens)
 
 
@@ -79,7 +74,7 @@ def test_forward_edge(wl):
         inp["logits"][:] = float("nan")
     out, inter, _ = PU.run_gpu(wl, inp)
     PU.check_routing_and_permutation(wl, inp, inter)
-    tokens = PU.sample_tokens(wl, inp, n=128)
+    tokens = PU.all_tokens(wl)
     ref, _, _ = PU.run_oracle(wl, inp, tokens)
     PU.check_outputs(wl, out, ref, tokens)
 
@@ -95,7 +90,7 @@ def test_all_tokens_on_the_same_experts():
     out, inter, _ = PU.run_gpu(wl, inp)
     PU.check_routing_and_permutation(wl, inp, inter)
     assert sorted(np.nonzero(inter["counts"])[0].tolist()) == [2, 5, 17, 60]
-    tokens = PU.sample_tokens(wl, inp, n=64)
+    tokens = PU.all_tokens(wl)
     ref, _, _ = PU.run_oracle(wl, inp, tokens)
     PU.check_outputs(wl, out, ref, tokens)
 

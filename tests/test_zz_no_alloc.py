@@ -1,9 +1,13 @@
 """The allocation-free entry point, moe_forward_noalloc, against moe_forward.
 
-Some callers cannot allocate device memory (allocator hooks, memory pools,
-hosts that forbid allocation after start-up); moe_forward_noalloc runs the
-same layer on a workspace that lives in the library's own device image.
-This file is collected last on purpose."""
+Some callers cannot allocate device memory: code that runs inside an
+allocator hook or a memory pool, and hosts that forbid device allocation
+after start-up.  moe_forward_noalloc runs the same layer on a workspace that
+lives in the library's own device image, and moe_check_noalloc reads that
+workspace's error word.  The two entry points launch the same deterministic
+kernels, so their outputs must agree bit for bit.  This file is collected
+last on purpose: a run that stops at its first failure has run every other
+test by then."""
 import numpy as np
 import pytest
 import torch
@@ -19,14 +23,23 @@ CASES = [
 ]
 
 
+def _lib_or_skip():
+    try:
+        return B.lib()
+    except (OSError, RuntimeError) as exc:  # no built library or no CUDA runtime here
+        pytest.skip(f"library not loadable: {exc}")
+
+
 def test_noalloc_rejects_oversized_plan_before_launch():
     # 4096 tokens x top-8 at H=2048 needs far more than the 16 MiB built in;
-    # rejected on the host, so this runs without a GPU too
-    B.lib()
+    # rejected on the host before anything touches a device
+    _lib_or_skip()
     p = B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_BF16)
     assert p.workspace_bytes > 16 << 20
     fake = 1 << 20
     rc = B.moe_forward_noalloc(p, fake, fake, fake, 0, fake, 0, fake, 0)
+    assert rc == B.MOE_ERR_WORKSPACE
+    rc, _ = B.moe_check_noalloc(p, 0)
     assert rc == B.MOE_ERR_WORKSPACE
 
 
@@ -41,7 +54,7 @@ def test_noalloc_matches_moe_forward_twice(wl):
     ref = layer.forward(x, lg)
     rc, bits = layer.check(wl.T)
     assert rc == 0, bits
-    ref = ref.float().cpu().double().numpy()
+    ref = ref.cpu()
     p = layer.plan(wl.T)
     assert p.workspace_bytes <= 16 << 20
     stream = torch.cuda.current_stream(dev).cuda_stream
@@ -52,8 +65,9 @@ def test_noalloc_matches_moe_forward_twice(wl):
             0 if layer.s13 is None else layer.s13.data_ptr(), layer.w2.data_ptr(),
             0 if layer.s2 is None else layer.s2.data_ptr(), out.data_ptr(), stream)
         assert rc == B.MOE_OK, B.strerror(rc)
-        torch.cuda.synchronize(dev)
-        got = out.float().cpu().double().numpy()
-        assert np.isfinite(got).all()
-        err = np.abs(got - ref).max()
-        assert err <= PU.TOL[wl.dtype] * np.abs(ref).max()
+        rc, bits = B.moe_check_noalloc(p, stream)
+        assert rc == B.MOE_OK and bits == 0, (rc, bits)
+        got = out.cpu()
+        # same kernels on the same inputs: identical bits, no tolerance
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+        assert np.isfinite(got.float().numpy()).all()
