@@ -271,7 +271,7 @@ class Runner:
                               scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2,
                               force_est=wl.force_est, ep_size=wl.ep_size, ep_rank=wl.ep_rank,
                               n_group=wl.n_group, topk_group=wl.topk_group,
-                              gemm_pair=wl.gemm_pair)
+                              gemm_pair=wl.gemm_pair, gemm_tm=wl.gemm_tm)
         self.x = inp["x"].to(dev)
         self.lg = inp["logits"].to(dev)
         self.out = torch.empty(wl.T, wl.H, dtype=self.x.dtype, device=dev)

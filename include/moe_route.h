@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 2
+#define MOE_ABI_VERSION 3
 
 /* return codes */
 #define MOE_OK 0
@@ -140,7 +140,13 @@ typedef struct moe_plan {
                          items of 256 weight rows; 0: one CTA per tile.  Set by
                          moe_plan; a caller may clear or set it (ignored for
                          FP8). */
-  int32_t reserved0;
+  int32_t gemm_tm;    /* FP8 only.  1: token-major grouped GEMMs -- every
+                         expert's rows in tiles of 128 on the MMA's M side,
+                         256 weight rows on its N side (gate and up rows of a
+                         128-feature block for GEMM 1, two 128-row blocks of
+                         w2 for GEMM 2); 0: weight rows on the M side and
+                         token tiles of tile_n.  Set by moe_plan when
+                         est >= 16; a caller may clear or set it. */
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;

@@ -122,4 +122,16 @@ cudaError_t launch_grouped_gemm_pair(int kind, int mode, const GemmArgs& args,
                                      const GemmMaps& maps, int smem_bytes, long long max_items,
                                      cudaStream_t stream);
 
+// Token-major FP8 grouped GEMMs (grouped_gemm_tm.cu): one stage holds two
+// 128-row weight boxes and a token box of up to 128 rows (128 bytes of K
+// each); outside the ring: alignment slack, barriers and the amax exchange.
+constexpr int kTmStageBytes = 3 * 16384;
+constexpr int kTmExtraSmem = 1024 + 512 + 4096;
+
+// Launch token-major GEMM1 (mode 1: gate+up with SiLU and e4m3 act) or
+// GEMM2 (mode 2: down with the routing weight) over `grid` persistent CTAs;
+// the token maps of `maps` are 16, 32, 64, 128 and 256 rows high.
+cudaError_t launch_grouped_gemm_tm(int mode, const GemmArgs& args, const GemmMaps& maps, int grid,
+                                   int smem_bytes, cudaStream_t stream);
+
 }  // namespace moe

@@ -39,6 +39,7 @@ constexpr int kRouteThreads = 256;  // 8 warps
 constexpr int kMaxK = 32;
 constexpr int kMaxE = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
+constexpr int kTmMinEst = 16;  // FP8 plans from this estimate on run token-major
 
 // ------------------------------------------------------------------ routing
 __device__ __forceinline__ float sanitize_logit(float v) {
@@ -777,17 +778,21 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   // rows than the tile), the kernel is one size wider (at most 64) and each
   // expert's tile grows to the rows it holds: fewer tiles, each weight block
   // streamed once per expert instead of once per tile.
+  // Token-major FP8 plans (gemm_tm) tile every expert's rows by 128: the
+  // tokens sit on the MMA's M side.
+  const bool tm = fp8 && p->gemm_tm != 0;
   const int fp8_nt = (fp8 && 2 * p->est > p->tile_n && p->tile_n < 64) ? 2 * p->tile_n : p->tile_n;
-  const int per_expert = fp8 ? (fp8_nt > p->tile_n ? 1 : 0) : 1;
+  const int per_expert = tm ? 0 : fp8 ? (fp8_nt > p->tile_n ? 1 : 0) : 1;
+  const int scan_tile = tm ? 128 : p->tile_n;
   // the largest tile the device may choose per GEMM.  One CTA per tile:
   // GEMM1 keeps two 2 x n-column accumulators in TMEM, so 128 is its widest
   // double-buffered tile; GEMM2 (one accumulator) widens hot experts to 256
   // tokens in prefill-sized plans (est > 64).  CTA pairs: 256 for both
   // (each CTA holds half of the tile's rows).
   const bool pair_plan = p->gemm_pair != 0 && !fp8;
-  const int NM1 = pair_plan ? 256 : fp8 ? fp8_nt : 128;
-  const int NM2 = pair_plan ? 256 : fp8 ? fp8_nt : (p->tile_n >= 128 ? 256 : 128);
-  launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, p->tile_n,
+  const int NM1 = tm ? 128 : pair_plan ? 256 : fp8 ? fp8_nt : 128;
+  const int NM2 = tm ? 128 : pair_plan ? 256 : fp8 ? fp8_nt : (p->tile_n >= 128 ? 256 : 128);
+  launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, scan_tile,
                  per_expert, NM1, NM2, p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
                  tiles2, ntiles2, dep, pair_plan ? 1 : 0, err);
   mark(2);
@@ -823,7 +828,34 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   if (sms <= 0) return MOE_ERR_CUDA;
   const int kb1 = H / (128 / esize), kb2 = I / (128 / esize);
   const int kbmax = kb1 > kb2 ? kb1 : kb2;
-  if (pair) {
+  if (tm) {
+    // token-major FP8: GEMM1 items are one 128-feature block (gate and up
+    // rows) x one 128-row token tile; GEMM2 items 256 output rows x one tile
+    GemmArgs g{};
+    g.p[0] = GemmPhase{tiles, ntiles, 2, 128, I / 128, H / 128, 2 * I, I, I, s13, 2 * I / 128, xs};
+    g.p[1] = GemmPhase{tiles, ntiles, 2, 256, (H + 255) / 256, I / 128, H, 128, H, s2, H / 128,
+                       as};
+    g.R = static_cast<int>(R);
+    g.act = act;
+    g.act_scale = as;
+    g.I = I;
+    g.src = src;
+    g.topw = topw;
+    g.ybuf = ybuf;
+    g.H = H;
+    g.err = err;
+    g.limit_ns = kWaitLimitNs;
+    const int st_max = (227 * 1024 - kTmExtraSmem) / kTmStageBytes;
+    g.stages = st_max > 8 ? 8 : st_max;
+    const int smem = g.stages * kTmStageBytes + kTmExtraSmem;
+    for (int mode = 1; mode <= 2; ++mode) {
+      const long long items = static_cast<long long>(p->max_tiles) * g.p[mode - 1].mblocks;
+      const int grid = static_cast<int>(items < sms ? items : sms);
+      if (launch_grouped_gemm_tm(mode, g, mode == 1 ? m1 : m2, grid, smem, st) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      mark(3 + mode);
+    }
+  } else if (pair) {
     // CTA pairs: half-height token maps, items of 256 weight rows, one
     // token tile list (widths up to 256) for both GEMMs
     const GemmMaps& h1 = ms.h1;
@@ -1043,6 +1075,8 @@ int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int r
   if (dtype == MOE_DTYPE_FP8_BLOCK128 && p.tile_n > 64) p.tile_n = 64;
   // experts with more than 32 rows on average: BF16/F32 GEMMs on CTA pairs
   p.gemm_pair = (dtype != MOE_DTYPE_FP8_BLOCK128 && p.est > 32) ? 1 : 0;
+  // FP8 with 16 or more rows per expert on average: token-major GEMMs
+  p.gemm_tm = (dtype == MOE_DTYPE_FP8_BLOCK128 && p.est >= kTmMinEst) ? 1 : 0;
   *plan = p;
   return MOE_OK;
 }
@@ -1053,12 +1087,14 @@ int moe_plan_describe(const moe_plan_t* p, char* buf, size_t n) {
   int len = std::snprintf(
       buf, buf ? n : 0,
       "moe_plan T=%d H=%d I=%d E=%d (ep %d/%d, %d local) k=%d dtype=%s scoring=%s renorm=%d "
-      "est=%d%s tile_n=%d route_tpc=%d chunks=%d max_tiles=%d g1_blocks=%d g2_blocks=%d "
-      "workspace=%llu B",
+      "est=%d%s tile_n=%d gemm=%s route_tpc=%d chunks=%d max_tiles=%d g1_blocks=%d "
+      "g2_blocks=%d workspace=%llu B",
       p->T, p->H, p->I, p->E, p->ep_rank, p->ep_size, p->e_local, p->k, dn[p->dtype],
       p->scoring ? "sigmoid" : "softmax", p->renorm,
-      p->est, p->force_est ? " (forced)" : "", p->tile_n, p->route_tpc, p->n_chunks,
-      p->max_tiles, p->g1_mblocks, p->g2_mblocks,
+      p->est, p->force_est ? " (forced)" : "", p->tile_n,
+      (p->dtype == MOE_DTYPE_FP8_BLOCK128 && p->gemm_tm) ? "token-major"
+      : (p->dtype != MOE_DTYPE_FP8_BLOCK128 && p->gemm_pair) ? "cta-pair" : "swap-ab",
+      p->route_tpc, p->n_chunks, p->max_tiles, p->g1_mblocks, p->g2_mblocks,
       static_cast<unsigned long long>(p->workspace_bytes));
   return len;
 }

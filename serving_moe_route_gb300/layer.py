@@ -37,11 +37,13 @@ class MoELayer:
     workspace per batch size, ``forward(x, logits) -> out``."""
 
     def __init__(self, w13, w2, *, k, dtype, scoring=SOFTMAX, renorm=True, s13=None, s2=None,
-                 force_est=0, ep_size=1, ep_rank=0, n_group=1, topk_group=1, gemm_pair=None):
+                 force_est=0, ep_size=1, ep_rank=0, n_group=1, topk_group=1, gemm_pair=None,
+                 gemm_tm=None):
         """w13/w2 (and s13/s2) hold this expert-parallel rank's experts: all
         of them when ep_size == 1, else E/ep_size of E = w13.shape[0] * ep_size;
         forward() then returns this rank's partial sum.  gemm_pair=None keeps
-        the plan's choice of CTA-pair GEMMs; 0 or 1 overrides it."""
+        the plan's choice of CTA-pair GEMMs (BF16/F32), gemm_tm=None its
+        choice of token-major GEMMs (FP8); 0 or 1 overrides either."""
         E, I2, H = w13.shape  # experts held by this rank
         I = I2 // 2
         _need(w13, _W_DTYPE[dtype], (E, 2 * I, H), "w13")
@@ -55,6 +57,7 @@ class MoELayer:
         self.ep_size, self.ep_rank = ep_size, ep_rank
         self.n_group, self.topk_group = n_group, topk_group
         self.gemm_pair = gemm_pair
+        self.gemm_tm = gemm_tm
         self.dtype, self.scoring, self.renorm, self.force_est = dtype, scoring, renorm, force_est
         self.w13, self.w2, self.s13, self.s2 = w13, w2, s13, s2
         self.device = w13.device
@@ -71,6 +74,8 @@ class MoELayer:
                 B.moe_plan_set_groups(p, self.n_group, self.topk_group)
             if self.gemm_pair is not None:
                 p.gemm_pair = int(bool(self.gemm_pair))
+            if self.gemm_tm is not None:
+                p.gemm_tm = int(bool(self.gemm_tm))
             self._plans[T] = p
         return p
 

@@ -49,6 +49,7 @@ class Workload:
     n_group: int = 1  # group-limited routing (1 = off)
     topk_group: int = 1
     gemm_pair: object = None  # None: the plan's choice; 0 / 1: forced
+    gemm_tm: object = None  # FP8 token-major GEMMs: None the plan's choice; 0 / 1 forced
     extra: dict = field(default_factory=dict, compare=False, hash=False)
 
 
@@ -200,12 +201,12 @@ def make_inputs(wl: Workload) -> dict:
 
 def custom(name="custom", *, T, H, I, E, k, dtype, scoring=SOFTMAX, renorm=True, logits="normal",
            seed=7, force_est=0, ep_size=1, ep_rank=0, n_group=1, topk_group=1,
-           gemm_pair=None) -> Workload:
+           gemm_pair=None, gemm_tm=None) -> Workload:
     """An ad-hoc workload (edge cases in tests)."""
     return Workload(name=name, T=T, H=H, I=I, E=E, k=k, dtype=dtype, scoring=scoring,
                     renorm=renorm, logits=logits, seed=seed, force_est=force_est,
                     ep_size=ep_size, ep_rank=ep_rank, n_group=n_group, topk_group=topk_group,
-                    gemm_pair=gemm_pair)
+                    gemm_pair=gemm_pair, gemm_tm=gemm_tm)
 
 
 # ------------------------------------------------------------ numpy views

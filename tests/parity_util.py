@@ -48,7 +48,8 @@ def make_layer(wl, inp) -> MoELayer:
     return MoELayer(inp["w13"].to(dev), inp["w2"].to(dev), k=wl.k, dtype=wl.dtype,
                     scoring=wl.scoring, renorm=wl.renorm, s13=s13, s2=s2, force_est=wl.force_est,
                     ep_size=wl.ep_size, ep_rank=wl.ep_rank, n_group=wl.n_group,
-                    topk_group=wl.topk_group, gemm_pair=wl.gemm_pair)
+                    topk_group=wl.topk_group, gemm_pair=wl.gemm_pair,
+                    gemm_tm=wl.gemm_tm)
 
 
 def run_gpu(wl, inp, layer=None):
@@ -62,6 +63,7 @@ def run_gpu(wl, inp, layer=None):
     inter = {k: v.cpu().numpy().copy() for k, v in layer.intermediates(wl.T).items()}
     inter["tile_n"] = layer.plan(wl.T).tile_n
     inter["gemm_pair"] = layer.plan(wl.T).gemm_pair
+    inter["gemm_tm"] = layer.plan(wl.T).gemm_tm
     inter["est"] = layer.plan(wl.T).est
     return out.float().cpu().double().numpy(), inter, layer
 
@@ -114,8 +116,11 @@ def check_routing_and_permutation(wl, inp, inter):
     # experts average more than half a tile; then widths grow per expert too
     est = int(inter["est"])
     fp8_nt = 2 * tile_n if (2 * est > tile_n and tile_n < 64) else tile_n
+    tm = wl.dtype == W.FP8 and int(inter["gemm_tm"])
     if int(inter["gemm_pair"]) and wl.dtype != W.FP8:
         lists = [("tiles", "ntiles", 256)]
+    elif tm:  # token-major FP8: every expert's rows in tiles of 128
+        lists = [("tiles", "ntiles", 128)]
     elif wl.dtype == W.FP8:
         lists = [("tiles", "ntiles", fp8_nt)]
     else:
@@ -131,7 +136,9 @@ def check_routing_and_permutation(wl, inp, inter):
             c = counts[e]
             bucket = 16 if c <= 16 else 32 if c <= 32 else 64 if c <= 64 else 128 if c <= 128 \
                 else 256
-            if wl.dtype == W.FP8 and fp8_nt == tile_n:
+            if tm:
+                want = 128
+            elif wl.dtype == W.FP8 and fp8_nt == tile_n:
                 want = tile_n
             else:
                 want = min(n_max, max(tile_n, bucket))

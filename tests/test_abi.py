@@ -166,3 +166,15 @@ def test_plan_gemm_pair_choice(B):
     assert B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_FP8_BLOCK128).gemm_pair == 0
     assert B.moe_plan(300, 160, 96, 8, 2, B.MOE_DTYPE_F32).gemm_pair == 1
     assert B.moe_plan(288, 2048, 768, 400, 6, B.MOE_DTYPE_BF16, force_est=288).gemm_pair == 1
+
+
+def test_plan_gemm_tm_choice(B):
+    # token-major FP8 GEMMs once experts average 16 rows or more
+    fp8 = B.MOE_DTYPE_FP8_BLOCK128
+    assert B.moe_plan(256, 2048, 768, 128, 8, fp8).gemm_tm == 1    # est 16
+    assert B.moe_plan(4096, 2048, 768, 128, 8, fp8).gemm_tm == 1   # est 256
+    assert B.moe_plan(240, 2048, 768, 128, 8, fp8).gemm_tm == 0    # est 15
+    assert B.moe_plan(1, 2048, 768, 128, 8, fp8).gemm_tm == 0
+    assert B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).gemm_tm == 0
+    assert "token-major" in B.moe_plan(4096, 2048, 768, 128, 8, fp8).describe()
+    assert "cta-pair" in B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).describe()

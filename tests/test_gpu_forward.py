@@ -64,6 +64,21 @@ EDGE = [
     W.custom("fp8_wider_32", T=96, H=256, I=256, E=32, k=4, dtype=W.FP8, seed=48),
     W.custom("fp8_wider_64", T=192, H=256, I=256, E=32, k=4, dtype=W.FP8, seed=49,
              logits="nan_rows"),
+    # token-major FP8 GEMMs (tokens on the MMA's M side, 128-row tiles):
+    # forced on small and ragged shapes (partial tiles, every token box
+    # height, H not a multiple of 256 so GEMM2's last item has one valid
+    # 128-row block), a hot expert with many tiles, and the other FP8 path
+    # forced on a plan that would pick token-major
+    W.custom("tm_ragged", T=37, H=384, I=256, E=40, k=3, dtype=W.FP8, seed=63, gemm_tm=1),
+    W.custom("tm_small", T=1, H=256, I=128, E=8, k=2, dtype=W.FP8, seed=64, gemm_tm=1),
+    W.custom("tm_many_tiles", T=700, H=256, I=384, E=8, k=2, dtype=W.FP8, seed=65,
+             logits="nan_rows"),
+    W.custom("tm_concentrated", T=400, H=256, I=256, E=64, k=4, dtype=W.FP8, seed=66,
+             logits="concentrated"),
+    W.custom("tm_sigmoid", T=300, H=256, I=256, E=16, k=4, dtype=W.FP8, seed=67,
+             scoring=W.SIGMOID),
+    W.custom("swap_ab_large_fp8", T=700, H=256, I=384, E=8, k=2, dtype=W.FP8, seed=65,
+             gemm_tm=0),
 ]
 
 
