@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the per-workload sweep and the routing micro-benchmark")
     ap.add_argument("--sweep-samples", type=int, default=24)
+    ap.add_argument("--sweep-only", default="",
+                    help="comma-separated workload names: sweep only these")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -558,8 +560,9 @@ def routing_bench(dev, calls=500):
     return out
 
 
-def sweep(dev, samples, pk):
-    """Every workload: median/p20/p80 us per call, tokens/s, roofline."""
+def sweep(dev, samples, pk, only=()):
+    """Every workload (or those in `only`): median/p20/p80 us per call,
+    tokens/s, roofline."""
     import torch
 
     from serving_moe_route_gb300 import workloads as W
@@ -567,6 +570,8 @@ def sweep(dev, samples, pk):
     wkey, weights = None, None
     rows = []
     for name in SWEEP:
+        if only and name not in only:
+            continue
         wl = wls[name]
         key = (wl.H, wl.I, wl.E, wl.dtype, wl.seed, wl.ep_size, wl.ep_rank)
         if key != wkey:  # weights depend on (H, I, E, dtype, seed, ep slice) only
@@ -705,7 +710,8 @@ def run_ours(args):
                          "source": pk["source"]}
         line["routing_microbench"] = routing_bench(dev)
         t0 = time.perf_counter()
-        line["sweep"] = sweep(dev, args.sweep_samples, pk)
+        only = tuple(n for n in args.sweep_only.split(",") if n)
+        line["sweep"] = sweep(dev, args.sweep_samples, pk, only)
         line["sweep_wall_s"] = round(time.perf_counter() - t0, 1)
         line["estimate_ablation"] = estimate_ablation(line["sweep"])
     if rank == 0:

@@ -23,7 +23,8 @@
 //                128-byte K block (the token box is only as high as the
 //                tile's rows need; rows past it are never stored)
 //   warp 1       TMEM allocation and the single-thread MMA issuer
-//   warps 2..17  epilogue: four warps per TMEM lane quadrant, each holding
+//   warps 2, 3   idle (they complete warp group 0's register hand-back)
+//   warps 4..19  epilogue: four warps per TMEM lane quadrant, each holding
 //                32 columns of both 128-column halves of its rows
 //                GEMM1: act = SiLU(gate) * up, then e4m3 per token and
 //                       128-feature group (the group's amax meets across the
@@ -43,9 +44,23 @@
 
 namespace moe {
 
+// Warp group 0 (warps 0..3): TMA producer, MMA issuer and two idle warps;
+// warp groups 1..4: the 16 epilogue warps.  Launched at 96 registers per
+// thread (640 threads: 61,440), warp group 0 gives registers back down to 64
+// and the epilogue takes them up to 104: 128 x 64 + 512 x 104 = 61,440, and
+// every SM sub-partition holds one warp of group 0 and four epilogue warps,
+// so the split balances there too (the epilogue's two 16-column TMEM loads
+// and 64 accumulators fit in 104 without spilling).
+constexpr int kTmRegsLaunch = 96;
+constexpr int kTmRegsGroup0 = 64;
+constexpr int kTmRegsEpilogue = 104;
 constexpr int kTmEpiWarps = 16;
-constexpr int kTmThreads = 64 + 32 * kTmEpiWarps;
+constexpr int kTmEpiWarp0 = 4;  // first epilogue warp
+constexpr int kTmThreads = 32 * (kTmEpiWarp0 + kTmEpiWarps);
 constexpr int kTmCols = 32;  // columns per epilogue thread in each 128-column half
+static_assert(128 * kTmRegsGroup0 + 32 * kTmEpiWarps * kTmRegsEpilogue ==
+                  kTmThreads * kTmRegsLaunch,
+              "the register split must hand out exactly the launch's registers");
 
 // the smallest token box (16, 32, 64 or 128 rows) that holds `rows`
 __device__ __forceinline__ int tm_box_rows(int rows) {
@@ -126,6 +141,9 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   int never = 0;
   bool ok = true;
 
+  if (warp < kTmEpiWarp0) {
+    // warp group 0 hands registers back before its roles start
+    setmaxnreg_dec<kTmRegsGroup0>();
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -206,9 +224,11 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       mbar_wait(smem_u32(done), 0, limit, &never);
     }
     __syncwarp();
+  }
   } else {
     // ------------------------------------------------------------ epilogue
-    const int ew = warp - 2;
+    setmaxnreg_inc<kTmRegsEpilogue>();
+    const int ew = warp - kTmEpiWarp0;
     const int q = warp & 3;    // TMEM lane quadrant this warp may read
     const int part = ew >> 2;  // which 32 columns of each 128-column half
     const int r = q * 32 + lane;  // this thread's token row within the tile
@@ -246,15 +266,18 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       float wt = 0.0f;  // GEMM2: the routing weight of this row's pick
       if (G == 1 && live) wt = __ldg(args.topw + __ldg(args.src + grow));
 
-      float acc0[kTmCols], acc1[kTmCols];
+      // accumulators as pairs of columns: the fold is one packed two-lane
+      // FMA (each lane rounded exactly like fmaf) per pair of columns
+      float2 acc0[kTmCols / 2], acc1[kTmCols / 2];
 #pragma unroll
-      for (int c = 0; c < kTmCols; ++c) {
-        acc0[c] = 0.0f;
-        acc1[c] = 0.0f;
+      for (int c = 0; c < kTmCols / 2; ++c) {
+        acc0[c] = make_float2(0.0f, 0.0f);
+        acc1[c] = make_float2(0.0f, 0.0f);
       }
       float sx_n = __ldg(sxp), sw0_n = __ldg(sw0p), sw1_n = __ldg(sw1p);
       for (int kb = 0; kb < kbs; ++kb, ++kc) {
         const float c0 = sx_n * sw0_n, c1 = sx_n * sw1_n;
+        const float2 c02 = make_float2(c0, c0), c12 = make_float2(c1, c1);
         if (kb + 1 < kbs) {  // the next block's scales load under this block's fold
           sx_n = __ldg(sxp + kb + 1);
           sw0_n = __ldg(sw0p + kb + 1);
@@ -269,16 +292,19 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         tc_fence_after();
         const uint32_t a0 = lane_addr + slot * 256u + static_cast<uint32_t>(part * kTmCols);
         const uint32_t a1 = a0 + 128u;
+        // two rounds of 16 columns of both halves, one TMEM round trip each
 #pragma unroll
-        for (int c = 0; c < kTmCols; c += 8) {
-          float p0[8], p1[8];
-          tmem_ld8(a0 + c, p0);
-          tmem_ld8(a1 + c, p1);
+        for (int c = 0; c < kTmCols; c += 16) {
+          float p0[16], p1[16];
+          tmem_ld16(a0 + c, p0);
+          tmem_ld16(a1 + c, p1);
           tmem_wait_ld(p0, p1);
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
-            acc0[c + i] = fmaf(p0[i], c0, acc0[c + i]);
-            acc1[c + i] = fmaf(p1[i], c1, acc1[c + i]);
+            acc0[c / 2 + i] =
+                __ffma2_rn(make_float2(p0[2 * i], p0[2 * i + 1]), c02, acc0[c / 2 + i]);
+            acc1[c / 2 + i] =
+                __ffma2_rn(make_float2(p1[2 * i], p1[2 * i + 1]), c12, acc1[c / 2 + i]);
           }
         }
         tc_fence_before();
@@ -289,11 +315,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       if constexpr (G == 0) {
         // act = SiLU(gate) * up for this row's 32 features of the block,
         // then e4m3 over the block's 128 features with one scale per row
+        float act[kTmCols];
         float m = 0.0f;
 #pragma unroll
-        for (int c = 0; c < kTmCols; ++c) {
-          acc0[c] = silu_f(acc0[c]) * acc1[c];
-          m = fmaxf(m, fabsf(acc0[c]));
+        for (int c = 0; c < kTmCols / 2; ++c) {
+          act[2 * c] = silu_f(acc0[c].x) * acc1[c].x;
+          act[2 * c + 1] = silu_f(acc0[c].y) * acc1[c].y;
+          m = fmaxf(m, fmaxf(fabsf(act[2 * c]), fabsf(act[2 * c + 1])));
         }
         float* rb = red + (ib & 1u) * 512;
         rb[part * 128 + r] = m;
@@ -313,8 +341,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
                          mb * 128 + part * kTmCols;
 #pragma unroll
           for (int c = 0; c < kTmCols; c += 16) {
-            const uint2 lo = pack_e4m3x8(acc0 + c, inv);
-            const uint2 hi = pack_e4m3x8(acc0 + c + 8, inv);
+            const uint2 lo = pack_e4m3x8(act + c, inv);
+            const uint2 hi = pack_e4m3x8(act + c + 8, inv);
             *reinterpret_cast<uint4*>(dst + c) = make_uint4(lo.x, lo.y, hi.x, hi.y);
           }
         }
@@ -328,15 +356,15 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           for (int half = 0; half < 2; ++half) {
             const int h = h0 + half * 128;
             if (h < args.H) {
-              const float* a = half ? acc1 : acc0;
+              const float2* a = half ? acc1 : acc0;
 #pragma unroll
-              for (int c = 0; c < kTmCols; c += 8) {
+              for (int c = 0; c < kTmCols / 2; c += 4) {
                 uint4 v;
-                v.x = pack_bf16x2(wt * a[c], wt * a[c + 1]);
-                v.y = pack_bf16x2(wt * a[c + 2], wt * a[c + 3]);
-                v.z = pack_bf16x2(wt * a[c + 4], wt * a[c + 5]);
-                v.w = pack_bf16x2(wt * a[c + 6], wt * a[c + 7]);
-                *reinterpret_cast<uint4*>(y + h + c) = v;
+                v.x = pack_bf16x2(wt * a[c].x, wt * a[c].y);
+                v.y = pack_bf16x2(wt * a[c + 1].x, wt * a[c + 1].y);
+                v.z = pack_bf16x2(wt * a[c + 2].x, wt * a[c + 2].y);
+                v.w = pack_bf16x2(wt * a[c + 3].x, wt * a[c + 3].y);
+                *reinterpret_cast<uint4*>(y + h + 2 * c) = v;
               }
             }
           }
@@ -363,11 +391,22 @@ static cudaError_t launch_tm_mode(const GemmArgs& args, const GemmMaps& maps, in
   // again after a switch of device); host threads may launch concurrently
   static std::mutex mu;
   static int configured = 0, conf_dev = -1;
+  static bool regs_checked = false;
   {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     std::lock_guard<std::mutex> lock(mu);
+    if (!regs_checked) {
+      // the register split hands out exactly the registers of a launch at
+      // kTmRegsLaunch per thread; with fewer, the epilogue's increase could
+      // never be granted, so such a build is refused rather than launched
+      cudaFuncAttributes fa;
+      e = cudaFuncGetAttributes(&fa, kern);
+      if (e != cudaSuccess) return e;
+      if (fa.numRegs != kTmRegsLaunch) return cudaErrorInvalidConfiguration;
+      regs_checked = true;
+    }
     if (dev != conf_dev || configured < smem) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (e != cudaSuccess) return e;

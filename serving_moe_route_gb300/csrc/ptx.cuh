@@ -274,6 +274,19 @@ __device__ __forceinline__ void tmem_wait_ld(float (&a)[N], float (&b)[N], float
   for (int i = 0; i < N; ++i) asm volatile("" : "+f"(a[i]), "+f"(b[i]), "+f"(c[i]), "+f"(d[i]));
 }
 
+// Register reallocation between warp groups: executed by all threads of a
+// warp group (4 consecutive warps) together; N a multiple of 8 in [24, 256].
+// The sum over the CTA's warp groups must stay within the registers the CTA
+// was launched with.
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 // named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads)
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
