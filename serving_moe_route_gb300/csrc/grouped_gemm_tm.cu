@@ -67,6 +67,41 @@ __device__ __forceinline__ int tm_box_rows(int rows) {
   return rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128;
 }
 
+// SiLU(z) = z * sigmoid(z) with sigmoid(z) = (1 + tanh(z/2)) / 2: one
+// hardware tanh approximation (relative error about 2^-11, far below the
+// e4m3 step the result is quantised to) instead of an exponential and a
+// reciprocal; large negative z give 0, large positive z give z
+__device__ __forceinline__ float silu_tanh(float z) {
+  const float h = 0.5f * z;
+  float t;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(h));
+  return fmaf(h, t, h);
+}
+
+// Shared-memory byte offset of 16-byte chunk `c` of row `r` in a tile of
+// 128-byte rows laid out with the 128-byte swizzle (the layout a TMA tensor
+// map with CU_TENSOR_MAP_SWIZZLE_128B reads): the chunk index is XORed with
+// the row's position in its 8-row (1024-byte) group.  Tiles start on
+// 1024-byte boundaries.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int c) {
+  return static_cast<uint32_t>(r) * 128u + static_cast<uint32_t>((c ^ (r & 7)) << 4);
+}
+
+// TMA stores of rows [0, n16) of a staged tile (n16 a multiple of 16, at most
+// 128) to rows row0.. of the tensor, column x: one box per set bit of n16
+// (128 / 64 / 32 / 16 rows), so that no row past the tile's own is written.
+__device__ __forceinline__ void store_rows16(const GemmMaps& out, uint32_t stg, int n16, int x,
+                                             int row0) {
+  int r0 = 0;
+#pragma unroll
+  for (int h = 128; h >= 16; h >>= 1) {
+    if (n16 & h) {
+      tma_store_2d(&out.b[tok_map_index(h)], stg + static_cast<uint32_t>(r0) * 128u, x, row0 + r0);
+      r0 += h;
+    }
+  }
+}
+
 // eight values -> eight e4m3 codes (clamped to +-448 first), little-endian
 __device__ __forceinline__ uint2 pack_e4m3x8(const float* v, float inv_scale) {
   uint2 out = make_uint2(0u, 0u);
@@ -84,7 +119,8 @@ __device__ __forceinline__ uint2 pack_e4m3x8(const float* v, float inv_scale) {
 
 template <int MODE>
 __global__ void __launch_bounds__(kTmThreads, 1)
-    moe_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const GemmArgs args) {
+    moe_gemm_tm_kernel(const __grid_constant__ GemmMaps maps, const __grid_constant__ GemmMaps omaps,
+                       const GemmArgs args) {
   constexpr int G = MODE - 1;  // which GEMM
   extern __shared__ uint8_t smem_raw[];
 
@@ -97,7 +133,11 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* full = reinterpret_cast<uint64_t*>(stages + static_cast<size_t>(S) * kTmStageBytes);
+  // output staging for the TMA stores: GEMM1 one 128-row x 128-byte act
+  // block, GEMM2 one 128-column half of the item's y rows (two 64-column
+  // boxes of 128 rows); both 128-byte swizzled
+  uint8_t* stg = stages + static_cast<size_t>(S) * kTmStageBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(stg + tm_out_bytes(MODE));
   uint64_t* empty = full + S;
   uint64_t* accf = empty + S;  // [2] K-block slot written by the MMAs
   uint64_t* acce = accf + 2;   // [2] K-block slot folded by the epilogue
@@ -125,7 +165,10 @@ __global__ void __launch_bounds__(kTmThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&maps.a);
-    for (int j = 0; j < kTokMaps; ++j) prefetch_tmap(&maps.b[j]);
+    for (int j = 0; j < kTokMaps; ++j) {
+      prefetch_tmap(&maps.b[j]);
+      prefetch_tmap(&omaps.b[j]);
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), 512);
@@ -292,15 +335,17 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         tc_fence_after();
         const uint32_t a0 = lane_addr + slot * 256u + static_cast<uint32_t>(part * kTmCols);
         const uint32_t a1 = a0 + 128u;
-        // two rounds of 16 columns of both halves, one TMEM round trip each
+        // rounds of FC columns of both halves, one TMEM round trip each (GEMM2
+        // keeps more state live across the loop and takes narrower rounds)
+        constexpr int FC = G == 0 ? 16 : 8;
 #pragma unroll
-        for (int c = 0; c < kTmCols; c += 16) {
-          float p0[16], p1[16];
-          tmem_ld16(a0 + c, p0);
-          tmem_ld16(a1 + c, p1);
+        for (int c = 0; c < kTmCols; c += FC) {
+          float p0[FC], p1[FC];
+          tmem_ld<FC>(a0 + c, p0);
+          tmem_ld<FC>(a1 + c, p1);
           tmem_wait_ld(p0, p1);
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
+          for (int i = 0; i < FC / 2; ++i) {
             acc0[c / 2 + i] =
                 __ffma2_rn(make_float2(p0[2 * i], p0[2 * i + 1]), c02, acc0[c / 2 + i]);
             acc1[c / 2 + i] =
@@ -312,6 +357,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       }
       if (!ok) break;
 
+      const bool elected = ew == 0 && lane == 0;  // issues the TMA stores
+      const int n16 = nrows & ~15;  // rows stored by TMA; the rest by their threads
       if constexpr (G == 0) {
         // act = SiLU(gate) * up for this row's 32 features of the block,
         // then e4m3 over the block's 128 features with one scale per row
@@ -319,12 +366,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         float m = 0.0f;
 #pragma unroll
         for (int c = 0; c < kTmCols / 2; ++c) {
-          act[2 * c] = silu_f(acc0[c].x) * acc1[c].x;
-          act[2 * c + 1] = silu_f(acc0[c].y) * acc1[c].y;
+          act[2 * c] = silu_tanh(acc0[c].x) * acc1[c].x;
+          act[2 * c + 1] = silu_tanh(acc0[c].y) * acc1[c].y;
           m = fmaxf(m, fmaxf(fabsf(act[2 * c]), fabsf(act[2 * c + 1])));
         }
         float* rb = red + (ib & 1u) * 512;
         rb[part * 128 + r] = m;
+        if (elected) bulk_wait_read<0>();  // the previous item's store has read the staging
         if (!ep_barrier()) {
           ok = false;
           break;
@@ -334,43 +382,75 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         // v / scale as v * (1 / scale): at most one fp32 ulp apart, far
         // below the e4m3 step
         const float inv = __frcp_rn(scale);
-        if (live) {
-          const int groups = args.I / 128;
-          if (part == 0) args.act_scale[static_cast<size_t>(grow) * groups + mb] = scale;
-          uint8_t* dst = static_cast<uint8_t*>(args.act) + static_cast<size_t>(grow) * args.I +
-                         mb * 128 + part * kTmCols;
+        uint4 v[2];
 #pragma unroll
-          for (int c = 0; c < kTmCols; c += 16) {
-            const uint2 lo = pack_e4m3x8(act + c, inv);
-            const uint2 hi = pack_e4m3x8(act + c + 8, inv);
-            *reinterpret_cast<uint4*>(dst + c) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+        for (int h = 0; h < 2; ++h) {
+          const uint2 lo = pack_e4m3x8(act + 16 * h, inv);
+          const uint2 hi = pack_e4m3x8(act + 16 * h + 8, inv);
+          v[h] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          *reinterpret_cast<uint4*>(stg + sw128_offset(r, 2 * part + h)) = v[h];
+        }
+        if (live) {
+          if (part == 0)
+            args.act_scale[static_cast<size_t>(grow) * (args.I / 128) + mb] = scale;
+          if (r >= n16) {  // the tile's last rows past a multiple of 16
+            uint8_t* dst = static_cast<uint8_t*>(args.act) + static_cast<size_t>(grow) * args.I +
+                           mb * 128 + part * kTmCols;
+            reinterpret_cast<uint4*>(dst)[0] = v[0];
+            reinterpret_cast<uint4*>(dst)[1] = v[1];
           }
         }
+        fence_proxy_async_shared();
+        if (!ep_barrier()) {
+          ok = false;
+          break;
+        }
+        if (elected && n16 > 0) {
+          store_rows16(omaps, smem_u32(stg), n16, mb * 128, row0);
+          bulk_commit();
+        }
       } else {
-        // weighted rows of the two output blocks, bf16
-        if (live) {
-          __nv_bfloat16* y = static_cast<__nv_bfloat16*>(args.ybuf) + static_cast<size_t>(grow) *
-                                                                        args.H;
-          const int h0 = mb * 256 + part * kTmCols;
+        // weighted rows of the two output blocks, bf16, one 128-column half
+        // per round through the staging buffer
+        auto store_half = [&](const float2(&a)[kTmCols / 2], int half) -> bool {
+          const int h0 = mb * 256 + half * 128;  // first column of this half
+          if (h0 >= args.H) return true;         // uniform: the block past H
+          if (elected) bulk_wait_read<0>();      // the staging is free again
+          if (!ep_barrier()) return false;
+          uint8_t* box = stg + (part >> 1) * 16384;  // this thread's 64-column box
+          uint4 v[4];
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const int h = h0 + half * 128;
-            if (h < args.H) {
-              const float2* a = half ? acc1 : acc0;
-#pragma unroll
-              for (int c = 0; c < kTmCols / 2; c += 4) {
-                uint4 v;
-                v.x = pack_bf16x2(wt * a[c].x, wt * a[c].y);
-                v.y = pack_bf16x2(wt * a[c + 1].x, wt * a[c + 1].y);
-                v.z = pack_bf16x2(wt * a[c + 2].x, wt * a[c + 2].y);
-                v.w = pack_bf16x2(wt * a[c + 3].x, wt * a[c + 3].y);
-                *reinterpret_cast<uint4*>(y + h + 2 * c) = v;
-              }
-            }
+          for (int i = 0; i < 4; ++i) {
+            v[i].x = pack_bf16x2(wt * a[4 * i].x, wt * a[4 * i].y);
+            v[i].y = pack_bf16x2(wt * a[4 * i + 1].x, wt * a[4 * i + 1].y);
+            v[i].z = pack_bf16x2(wt * a[4 * i + 2].x, wt * a[4 * i + 2].y);
+            v[i].w = pack_bf16x2(wt * a[4 * i + 3].x, wt * a[4 * i + 3].y);
+            *reinterpret_cast<uint4*>(box + sw128_offset(r, (part & 1) * 4 + i)) = v[i];
           }
+          if (live && r >= n16) {  // the tile's last rows past a multiple of 16
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.ybuf) +
+                                                  static_cast<size_t>(grow) * args.H + h0 +
+                                                  part * kTmCols);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) dst[i] = v[i];
+          }
+          fence_proxy_async_shared();
+          if (!ep_barrier()) return false;
+          if (elected && n16 > 0) {
+            store_rows16(omaps, smem_u32(stg), n16, h0, row0);
+            store_rows16(omaps, smem_u32(stg + 16384), n16, h0 + 64, row0);
+            bulk_commit();
+          }
+          return true;
+        };
+        if (!store_half(acc0, 0) || !store_half(acc1, 1)) {
+          ok = false;
+          break;
         }
       }
     }
+    // every store has landed before the CTA leaves
+    if (ew == 0 && lane == 0) bulk_wait<0>();
     if (!ok) {
       *abort_flag = 1;
       if (lane == 0) atomicOr(args.err, kDevErrTimeout);
@@ -384,8 +464,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 }
 
 template <int MODE>
-static cudaError_t launch_tm_mode(const GemmArgs& args, const GemmMaps& maps, int grid, int smem,
-                                  cudaStream_t stream) {
+static cudaError_t launch_tm_mode(const GemmArgs& args, const GemmMaps& maps,
+                                  const GemmMaps& omaps, int grid, int smem, cudaStream_t stream) {
   auto kern = moe_gemm_tm_kernel<MODE>;
   // max dynamic smem is a per-function attribute, raised once per size (and
   // again after a switch of device); host threads may launch concurrently
@@ -415,14 +495,16 @@ static cudaError_t launch_tm_mode(const GemmArgs& args, const GemmMaps& maps, in
     }
   }
   return launch_chained(kern, dim3(grid), dim3(kTmThreads), static_cast<size_t>(smem), stream,
-                        maps, args);
+                        maps, omaps, args);
 }
 
-cudaError_t launch_grouped_gemm_tm(int mode, const GemmArgs& args, const GemmMaps& maps, int grid,
-                                   int smem, cudaStream_t stream) {
-  if (args.stages < 1 || grid < 1) return cudaErrorInvalidValue;
-  return mode == 1 ? launch_tm_mode<1>(args, maps, grid, smem, stream)
-                   : launch_tm_mode<2>(args, maps, grid, smem, stream);
+cudaError_t launch_grouped_gemm_tm(int mode, const GemmArgs& args, const GemmMaps& maps,
+                                   const GemmMaps& omaps, int grid, int smem,
+                                   cudaStream_t stream) {
+  if (args.stages < 1 || grid < 1 || smem < tm_smem_bytes(mode, args.stages))
+    return cudaErrorInvalidValue;
+  return mode == 1 ? launch_tm_mode<1>(args, maps, omaps, grid, smem, stream)
+                   : launch_tm_mode<2>(args, maps, omaps, grid, smem, stream);
 }
 
 }  // namespace moe
