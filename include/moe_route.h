@@ -146,7 +146,7 @@ typedef struct moe_plan {
                          128-feature block for GEMM 1, two 128-row blocks of
                          w2 for GEMM 2); 0: weight rows on the M side and
                          token tiles of tile_n.  Set by moe_plan when
-                         est >= 16; a caller may clear or set it. */
+                         est >= 32; a caller may clear or set it. */
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;

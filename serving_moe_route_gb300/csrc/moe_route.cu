@@ -39,7 +39,7 @@ constexpr int kRouteThreads = 256;  // 8 warps
 constexpr int kMaxK = 32;
 constexpr int kMaxE = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
-constexpr int kTmMinEst = 16;  // FP8 plans from this estimate on run token-major
+constexpr int kTmMinEst = 32;  // FP8 plans from this estimate on run token-major
 
 // ------------------------------------------------------------------ routing
 __device__ __forceinline__ float sanitize_logit(float v) {
@@ -1082,7 +1082,7 @@ int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int r
   if (dtype == MOE_DTYPE_FP8_BLOCK128 && p.tile_n > 64) p.tile_n = 64;
   // experts with more than 32 rows on average: BF16/F32 GEMMs on CTA pairs
   p.gemm_pair = (dtype != MOE_DTYPE_FP8_BLOCK128 && p.est > 32) ? 1 : 0;
-  // FP8 with 16 or more rows per expert on average: token-major GEMMs
+  // FP8 with 32 or more rows per expert on average: token-major GEMMs
   p.gemm_tm = (dtype == MOE_DTYPE_FP8_BLOCK128 && p.est >= kTmMinEst) ? 1 : 0;
   *plan = p;
   return MOE_OK;

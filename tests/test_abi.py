@@ -169,11 +169,12 @@ def test_plan_gemm_pair_choice(B):
 
 
 def test_plan_gemm_tm_choice(B):
-    # token-major FP8 GEMMs once experts average 16 rows or more
+    # token-major FP8 GEMMs once experts average 32 rows or more
     fp8 = B.MOE_DTYPE_FP8_BLOCK128
-    assert B.moe_plan(256, 2048, 768, 128, 8, fp8).gemm_tm == 1    # est 16
+    assert B.moe_plan(512, 2048, 768, 128, 8, fp8).gemm_tm == 1    # est 32
     assert B.moe_plan(4096, 2048, 768, 128, 8, fp8).gemm_tm == 1   # est 256
-    assert B.moe_plan(240, 2048, 768, 128, 8, fp8).gemm_tm == 0    # est 15
+    assert B.moe_plan(496, 2048, 768, 128, 8, fp8).gemm_tm == 0    # est 31
+    assert B.moe_plan(256, 2048, 768, 128, 8, fp8).gemm_tm == 0    # est 16
     assert B.moe_plan(1, 2048, 768, 128, 8, fp8).gemm_tm == 0
     assert B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).gemm_tm == 0
     assert "token-major" in B.moe_plan(4096, 2048, 768, 128, 8, fp8).describe()

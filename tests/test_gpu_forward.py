@@ -74,7 +74,7 @@ EDGE = [
     W.custom("tm_many_tiles", T=700, H=256, I=384, E=8, k=2, dtype=W.FP8, seed=65,
              logits="nan_rows"),
     W.custom("tm_concentrated", T=400, H=256, I=256, E=64, k=4, dtype=W.FP8, seed=66,
-             logits="concentrated"),
+             logits="concentrated", gemm_tm=1),
     W.custom("tm_sigmoid", T=300, H=256, I=256, E=16, k=4, dtype=W.FP8, seed=67,
              scoring=W.SIGMOID),
     W.custom("swap_ab_large_fp8", T=700, H=256, I=384, E=8, k=2, dtype=W.FP8, seed=65,
