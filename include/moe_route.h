@@ -317,6 +317,55 @@ int moe_forward_noalloc(const moe_plan_t* plan, const void* x, const void* logit
  */
 int moe_check_noalloc(const moe_plan_t* plan, uint32_t* bits, void* stream);
 
+/*
+ * Expert parallelism across ranks (H20 article, para. 2: the fused-MoE call
+ * takes the expert-parallel size and rank; para. 3: 400 expert slots over
+ * 8 GPUs).  Each rank routes its own T tokens over all E = e_local * ep_size
+ * experts, sends every token once to each rank that owns at least one of its
+ * picks (owner = id / e_local), runs moe_forward_with_ids on an
+ * expert-parallel plan (moe_plan_ep) over the rows it receives, and sums the
+ * partial rows that come back.  The three calls below are that exchange's
+ * arithmetic; moving rows between ranks (an all-to-all) is the caller's.
+ * They are asynchronous on `stream` and allocate nothing; ep_size <= 32.
+ *
+ * moe_ep_dispatch -- the send plan.
+ *   ids          device int32 [T, k] global expert ids (picks outside
+ *                [0, E) are ignored)
+ *   send_counts  device int32 [ep_size] out: tokens sent to each rank
+ *   send_tokens  device int32 [T * ep_size] out: the sent tokens, grouped by
+ *                destination rank in rank order, each group in token order
+ *                (entries past the total are left as they were)
+ *   row_of       device int32 [T, ep_size] out: the send row of (token,
+ *                rank), or -1 when the token is not sent to that rank
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.
+ */
+int moe_ep_dispatch(const int32_t* ids, int T, int k, int e_local, int ep_size,
+                    int32_t* send_counts, int32_t* send_tokens, int32_t* row_of, void* stream);
+
+/*
+ * moe_ep_pack -- gather the send rows of moe_ep_dispatch's plan: send row r
+ * (r below the total of send_counts) receives token send_tokens[r]'s
+ * activation row (x [T, H], MOE_DTYPE_F32 or MOE_DTYPE_BF16), its k ids and
+ * its k weights (w device f32 [T, k]).  x_send [T * ep_size, H], ids_send
+ * [T * ep_size, k] and w_send [T * ep_size, k] are the caller's buffers;
+ * rows past the total are not written.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.
+ */
+int moe_ep_pack(const void* x, int x_dtype, const int32_t* ids, const float* w, int T, int H,
+                int k, int ep_size, const int32_t* send_counts, const int32_t* send_tokens,
+                void* x_send, int32_t* ids_send, float* w_send, void* stream);
+
+/*
+ * moe_ep_combine -- the layer's output from the partial rows that came back
+ * (back device f32 [n, H], row r the owner's partial sum for send row r):
+ * out[t] = sum over d = 0, 1, ..., ep_size-1 with row_of[t, d] >= 0 of
+ * back[row_of[t, d]], added in that (rank) order, so the result does not
+ * depend on arrival order; a token with no row gets zeros.  out device f32
+ * [T, H].  Errors: MOE_ERR_INVALID_ARG, MOE_ERR_CUDA.
+ */
+int moe_ep_combine(const float* back, const int32_t* row_of, int T, int H, int ep_size,
+                   float* out, void* stream);
+
 /* moe_strerror -- static message for a MOE_* return code. */
 const char* moe_strerror(int code);
 

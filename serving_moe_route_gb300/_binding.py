@@ -30,6 +30,7 @@ MOE_SCORING_SOFTMAX, MOE_SCORING_SIGMOID = 0, 1
 EXPORTED = ("moe_plan", "moe_plan_ep", "moe_forward", "moe_forward_timed", "moe_forward_with_ids",
             "moe_forward_noalloc", "moe_check_noalloc", "moe_route_topk", "moe_route_grouped_topk",
             "moe_plan_set_groups", "moe_check", "moe_plan_describe",
+            "moe_ep_dispatch", "moe_ep_pack", "moe_ep_combine",
             "moe_strerror", "moe_abi_version")
 
 
@@ -108,6 +109,12 @@ def lib() -> ctypes.CDLL:
     L.moe_route_topk.restype = i
     L.moe_check.argtypes = [ctypes.POINTER(MoePlan), P, ctypes.POINTER(c_u32), P]
     L.moe_check.restype = i
+    L.moe_ep_dispatch.argtypes = [P, i, i, i, i, P, P, P, P]
+    L.moe_ep_dispatch.restype = i
+    L.moe_ep_pack.argtypes = [P, i, P, P, i, i, i, i, P, P, P, P, P, P]
+    L.moe_ep_pack.restype = i
+    L.moe_ep_combine.argtypes = [P, P, i, i, i, P, P]
+    L.moe_ep_combine.restype = i
     if L.moe_abi_version() != 3:
         raise RuntimeError("libmoe_route ABI version mismatch")
     _lib = L
@@ -194,3 +201,18 @@ def moe_check(plan, ws, stream):
     bits = c_u32(0)
     rc = lib().moe_check(ctypes.byref(plan), ws, ctypes.byref(bits), stream)
     return rc, bits.value
+
+
+def moe_ep_dispatch(ids, T, k, e_local, ep_size, send_counts, send_tokens, row_of, stream):
+    return lib().moe_ep_dispatch(ids, T, k, e_local, ep_size, send_counts, send_tokens, row_of,
+                                 stream)
+
+
+def moe_ep_pack(x, x_dtype, ids, w, T, H, k, ep_size, send_counts, send_tokens, x_send, ids_send,
+                w_send, stream):
+    return lib().moe_ep_pack(x, x_dtype, ids, w, T, H, k, ep_size, send_counts, send_tokens,
+                             x_send, ids_send, w_send, stream)
+
+
+def moe_ep_combine(back, row_of, T, H, ep_size, out, stream):
+    return lib().moe_ep_combine(back, row_of, T, H, ep_size, out, stream)

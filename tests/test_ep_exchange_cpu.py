@@ -1,8 +1,10 @@
 """Expert parallelism across ranks on CPU: two gloo ranks run ep_forward
-(route, all-to-all dispatch, local slice, all-to-all combine); the output
-for each rank's tokens must equal the oracle's full layer.  The local slice
-here is a float64 dense reference of the rank's own experts; on GPUs it is an
-expert-parallel MoELayer."""
+(route, send plan, all-to-all dispatch, local slice, all-to-all return,
+combine); the output for each rank's tokens must equal the oracle's full
+layer.  The local slice here is a float64 dense reference of the rank's own
+experts, and the send plan, packing and combine are the plain-torch reference
+of tests/ep_reference.py; on GPUs they are an expert-parallel MoELayer and
+the library's moe_ep_* calls."""
 import os
 import socket
 import sys
@@ -28,11 +30,13 @@ def _silu(z):
 
 def _rank_main(rank, world, port, split, q):
     sys.path.insert(0, ROOT)
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
         import oracle
         from serving_moe_route_gb300 import workloads as W
+        from ep_reference import TorchEpOps
         from serving_moe_route_gb300.ep import ep_forward
 
         T, H, I, E, k = sum(split), 128, 64, 8, 2
@@ -62,7 +66,7 @@ def _rank_main(rank, world, port, split, q):
             return torch.from_numpy(out.astype(np.float32))
 
         got = ep_forward(x_all[tok].contiguous(), lg_all[tok].contiguous(), k=k, E=E,
-                         route=route, local_forward=local_forward)
+                         route=route, local_forward=local_forward, ops=TorchEpOps())
         ref, _, _ = oracle.moe_forward(
             T=T, H=H, I=I, E=E, k=k, dtype=wl.dtype, scoring=wl.scoring, renorm=wl.renorm,
             x=W.storage_numpy(inp["x"]), logits=W.storage_numpy(inp["logits"]),
