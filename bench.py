@@ -569,9 +569,7 @@ def sweep(dev, samples, pk, only=()):
     wls = W.workloads()
     wkey, weights = None, None
     rows = []
-    for name in SWEEP:
-        if only and name not in only:
-            continue
+    for name in (only or SWEEP):
         wl = wls[name]
         key = (wl.H, wl.I, wl.E, wl.dtype, wl.seed, wl.ep_size, wl.ep_rank)
         if key != wkey:  # weights depend on (H, I, E, dtype, seed, ep slice) only

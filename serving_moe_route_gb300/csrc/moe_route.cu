@@ -483,6 +483,7 @@ __device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
 
 // RB rows' loads in flight per lane: 4 for small batches (too few warps to
 // hide the load latency otherwise), 1 when the warps alone fill the GPU
+// (measured: eight in flight at T=4096 took 61 us against 35 with one)
 template <typename YT, int RB>
 __global__ void __launch_bounds__(256)
     combine_kernel(const YT* __restrict__ ybuf, const int* __restrict__ pos, int T, int H, int k,
