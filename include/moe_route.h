@@ -98,9 +98,8 @@ extern "C" {
  *   pos     int32 [T*k]     flat index -> permuted row (inverse of src)
  *   tiles   int32 [max_tiles, 4]  {expert, first row, rows, width} token
  *                           tiles of grouped GEMM 1, in expert order (CTA-pair
- *                           plans: the tiles of experts that fill a whole
- *                           256-row tile and the tiles of the other experts
- *                           merged at even rates, each group in expert order)
+ *                           plans: experts that fill a whole 256-row tile
+ *                           first, then the rest, each group in expert order)
  *   ntiles  int32 [1]       number of valid tiles
  *   tiles2, ntiles2         the same for grouped GEMM 2 when its widths differ
  *                           (prefill-sized BF16/F32 plans); otherwise unused

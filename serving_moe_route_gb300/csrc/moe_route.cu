@@ -284,36 +284,21 @@ __device__ __forceinline__ int expert_tile(int cnt, int tile_n, int per_expert, 
 // Writes one token-tile list per grouped GEMM: list 1 with widths up to
 // n_max1 (GEMM1), list 2 up to n_max2 (GEMM2); when the caps agree list 2
 // is not written and GEMM2 reads list 1.
-// With interleave, the tiles of experts that fill at least one whole tile
-// ("heavy", nh tiles) and the single tiles of the other experts ("light", nl
-// tiles) are merged at even rates: heavy tile i and light tile j are ordered
-// by (2i+1)*nl against (2j+1)*nh (ties to the heavy tile), each group in
-// expert order.  A grid-stride walk over the list then gives every CTA pair
-// a mix of heavy items, which keep the tensor pipe busy, and light items,
-// whose weight bytes keep HBM busy, instead of one phase of each.
-__device__ __forceinline__ int interleave_heavy(long long i, long long nh, long long nl) {
-  const long long num = (2 * i + 1) * nl - nh;  // light tiles with a smaller key
-  const long long before = num <= 0 ? 0 : (num + 2 * nh - 1) / (2 * nh);
-  return static_cast<int>(i + (before < nl ? before : nl));
-}
-__device__ __forceinline__ int interleave_light(long long j, long long nh, long long nl) {
-  const long long num = (2 * j + 1) * nh - nl;  // heavy tiles with a smaller or equal key
-  const long long before = num < 0 ? 0 : num / (2 * nl) + 1;
-  return static_cast<int>(j + (before < nh ? before : nh));
-}
-
+// With heavy_first, the experts that fill at least one whole tile come
+// first (in expert order), then the rest: a grid-stride walk over the list
+// then deals the long items out evenly before the short ones.
 __device__ void write_tile_list(int e, int E, int cnt, int off, int ne, int max_tiles,
-                               bool interleave, int* warp_sums, int* tot, int4* tiles,
+                               bool heavy_first, int* warp_sums, int* tot, int4* tiles,
                                int* ntiles, unsigned* err) {
   const int ntl = (cnt + ne - 1) / ne;
-  int tstart = 0;
-  __shared__ int tot_heavy, tot_light;
-  const bool heavy = cnt >= ne;
-  if (interleave) {
+  int tstart;
+  if (heavy_first) {
+    const bool heavy = cnt >= ne;
+    __shared__ int tot_heavy;
     const int hs = block_exclusive_scan(heavy ? ntl : 0, warp_sums, &tot_heavy);
-    const int ls = block_exclusive_scan(heavy ? 0 : ntl, warp_sums, &tot_light);
-    tstart = heavy ? hs : ls;
-    if (e == 0) *tot = tot_heavy + tot_light;
+    const int ls = block_exclusive_scan(heavy ? 0 : ntl, warp_sums, tot);
+    tstart = heavy ? hs : tot_heavy + ls;
+    if (e == 0) *tot += tot_heavy;
     __syncthreads();
   } else {
     tstart = block_exclusive_scan(ntl, warp_sums, tot);
@@ -323,12 +308,8 @@ __device__ void write_tile_list(int e, int E, int cnt, int off, int ne, int max_
     *ntiles = min(*tot, max_tiles);
   }
   if (e < E)
-    for (int i = 0; i < ntl; ++i) {
-      const int pos = !interleave ? tstart + i
-                      : heavy     ? interleave_heavy(tstart + i, tot_heavy, tot_light)
-                                  : interleave_light(tstart + i, tot_heavy, tot_light);
-      if (pos < max_tiles) tiles[pos] = make_int4(e, off + i * ne, min(ne, cnt - i * ne), ne);
-    }
+    for (int i = 0; i < ntl && tstart + i < max_tiles; ++i)
+      tiles[tstart + i] = make_int4(e, off + i * ne, min(ne, cnt - i * ne), ne);
 }
 
 __global__ void __launch_bounds__(1024)
@@ -337,7 +318,7 @@ __global__ void __launch_bounds__(1024)
                 int* __restrict__ chunk_base, int* __restrict__ counts,
                 int* __restrict__ offsets, int4* __restrict__ tiles1, int* __restrict__ ntiles1,
                 int4* __restrict__ tiles2, int* __restrict__ ntiles2, int* __restrict__ dep,
-                int interleave, unsigned* __restrict__ err) {
+                int heavy_first, unsigned* __restrict__ err) {
   __shared__ int warp_sums[32];
   pdl_trigger();
   pdl_wait();
@@ -358,10 +339,10 @@ __global__ void __launch_bounds__(1024)
   if (e < E) offsets[e] = off;
   if (e == 0) offsets[E] = tot_rows;
   write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max1), max_tiles,
-                  interleave != 0, warp_sums, &tot_tiles1, tiles1, ntiles1, err);
+                  heavy_first, warp_sums, &tot_tiles1, tiles1, ntiles1, err);
   if (n_max2 != n_max1)
     write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max2), max_tiles,
-                    interleave != 0, warp_sums, &tot_tiles2, tiles2, ntiles2, err);
+                    heavy_first, warp_sums, &tot_tiles2, tiles2, ntiles2, err);
 }
 
 // ------------------------------------------------------------------ gather
