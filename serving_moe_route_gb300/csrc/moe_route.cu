@@ -49,6 +49,19 @@ __device__ __forceinline__ float sanitize_logit(float v) {
   return v;
 }
 
+// Order-preserving unsigned key of a sanitised (finite) logit: a > b as
+// floats exactly when key(a) > key(b), with -0 taken as +0 (they compare
+// equal as floats).  Every finite value maps above 0, so 0 can stand for
+// "no candidate".  Warp maxima and minima of these keys are single
+// reduction instructions (redux.sync) instead of shuffle ladders.
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t b = __float_as_uint(v == 0.0f ? 0.0f : v);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t u) {
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7fffffffu) : ~u);
+}
+
 __device__ __forceinline__ float load_logit(const float* p) { return __ldg(p); }
 __device__ __forceinline__ float load_logit(const __nv_bfloat16* p) {
   return __bfloat162float(p[0]);
@@ -81,41 +94,34 @@ __global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
         const int e = i * 32 + lane;
         v[i] = (e < E) ? sanitize_logit(load_logit(logits + static_cast<size_t>(t) * E + e)) : 0.0f;
       }
+      uint32_t vk[VPT];  // the logits' order keys (0: no expert in this slot)
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) vk[i] = (i * 32 + lane < E) ? logit_key(v[i]) : 0u;
       uint32_t taken = 0;
       if (n_group > 1) {
-        // group-limited routing: lane g holds the largest sanitised logit of
-        // group g; keep the topk_group best groups (ties to the lower group)
-        // and exclude the other groups' experts from the top-k below
+        // group-limited routing: lane g holds the key of the largest
+        // sanitised logit of group g; keep the topk_group best groups (ties
+        // to the lower group) and exclude the other groups' experts below
         const int gs = E / n_group;
-        float my_gmax = -INFINITY;
+        uint32_t my_gkey = 0;
         for (int g = 0; g < n_group; ++g) {
-          float m = -INFINITY;
+          uint32_t m = 0;
 #pragma unroll
           for (int i = 0; i < VPT; ++i) {
             const int e = i * 32 + lane;
-            if (e < E && e / gs == g) m = fmaxf(m, v[i]);
+            if (e < E && e / gs == g) m = max(m, vk[i]);
           }
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-          if (lane == g) my_gmax = m;
+          m = __reduce_max_sync(0xffffffffu, m);
+          if (lane == g) my_gkey = m;
         }
         uint32_t kept = 0;
         bool mine_kept = false;
         for (int r = 0; r < topk_group; ++r) {
-          const bool avail = lane < n_group && !mine_kept;
-          float bv = avail ? my_gmax : -INFINITY;
-          int bi = avail ? lane : 0x7fffffff;
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-            if (ov > bv || (ov == bv && oi < bi)) {
-              bv = ov;
-              bi = oi;
-            }
-          }
-          kept |= 1u << bi;
-          if (lane == bi) mine_kept = true;
+          const uint32_t ck = (lane < n_group && !mine_kept) ? my_gkey : 0u;
+          const uint32_t kmax = __reduce_max_sync(0xffffffffu, ck);
+          const uint32_t g = __reduce_min_sync(0xffffffffu, (ck == kmax) ? lane : 0xffffffffu);
+          kept |= 1u << g;
+          if (lane == static_cast<int>(g)) mine_kept = true;
         }
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
@@ -125,30 +131,24 @@ __global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
       }
       float my_v = 0.0f;
       for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+        // this lane's best remaining expert (lane-local experts ascend with
+        // i, so '>' keeps the lower index on ties), then the warp's: the
+        // largest key, and among lanes holding it the lowest expert index
+        uint32_t bk = 0;
+        uint32_t bi = 0xffffffffu;
 #pragma unroll
         for (int i = 0; i < VPT; ++i) {
-          const int e = i * 32 + lane;
-          // lane-local experts ascend with i, so '>' keeps the lower index on ties
-          if (e < E && !((taken >> i) & 1u) && v[i] > bv) {
-            bv = v[i];
-            bi = e;
+          if (!((taken >> i) & 1u) && vk[i] > bk) {
+            bk = vk[i];
+            bi = static_cast<uint32_t>(i * 32 + lane);
           }
         }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-          const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-          if (ov > bv || (ov == bv && oi < bi)) {
-            bv = ov;
-            bi = oi;
-          }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+        const uint32_t best = __reduce_min_sync(0xffffffffu, (bk == kmax) ? bi : 0xffffffffu);
+        if ((best & 31u) == static_cast<uint32_t>(lane)) taken |= 1u << (best >> 5);
         if (lane == j) {
-          my_id = bi;
-          my_v = bv;
+          my_id = static_cast<int>(best);
+          my_v = key_logit(kmax);
         }
       }
       // weights

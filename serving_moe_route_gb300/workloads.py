@@ -74,7 +74,7 @@ def workloads() -> dict:
         w[f"fp8_T{T}"] = _wl(f"fp8_T{T}", T, 2048, 768, 128, 8, FP8, 1003)
     # the FP8 batch sweep's decode sizes with the token-major GEMMs forced
     # (the plan picks them from 32 rows per expert on)
-    for T in (16, 64, 128, 256):
+    for T in (1, 2, 4, 16, 64, 128, 256):
         w[f"fp8_T{T}_tm"] = _wl(f"fp8_T{T}_tm", T, 2048, 768, 128, 8, FP8, 1003, gemm_tm=1)
     # the H20 article's setting: 400 expert slots over 8 GPUs, local MoE of one rank
     w["sparse_uniform_bf16_ep8"] = _wl("sparse_uniform_bf16_ep8", 288, 2048, 768, 400, 6, BF16,

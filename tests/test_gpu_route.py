@@ -55,6 +55,13 @@ def test_route_edge_rows(E, k, scoring):
     lg[4, 0] = float("inf")
     lg[4, E - 1] = float("-inf")
     lg[5] = -1e30
+    # signed zeros tie (they compare equal), so the lower expert wins either way
+    lg[6] = -1.0
+    lg[6, 1::2] = 0.0
+    lg[6, 0::2] = -0.0
+    lg[7] = float("-inf")
+    lg[7, E - 1] = -0.0
+    lg[7, 0] = 0.0
     for dt in (torch.float32, torch.bfloat16):
         ids = _compare(lg.to(dt), k, scoring, True)
         assert list(ids[0]) == list(range(k))
