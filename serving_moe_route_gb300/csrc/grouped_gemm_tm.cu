@@ -28,8 +28,11 @@
 //                32 columns of both 128-column halves of its rows
 //                GEMM1: act = SiLU(gate) * up, then e4m3 per token and
 //                       128-feature group (the group's amax meets across the
-//                       four warps of a quadrant in shared memory)
-//                GEMM2: ybuf[row] = w[t,j] * y (the combine's weighting)
+//                       four warps of a quadrant in shared memory), staged
+//                       swizzled and written with TMA tensor stores
+//                GEMM2: ybuf[row] = w[t,j] * y (the combine's weighting),
+//                       each warp's rows turned around in its own shared
+//                       memory and written 8 rows x 64 bytes per store
 //
 // Every wait is bounded; a timeout sets MOE_DEVERR_TIMEOUT, raises a CTA
 // abort flag, drains in-flight copies and MMAs, frees TMEM and returns.
@@ -133,9 +136,8 @@ __global__ void __launch_bounds__(kTmThreads, 1)
 
   uint8_t* stages = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  // output staging for the TMA stores: GEMM1 one 128-row x 128-byte act
-  // block, GEMM2 one 128-column half of the item's y rows (two 64-column
-  // boxes of 128 rows); both 128-byte swizzled
+  // output staging: GEMM1 one 128-row x 128-byte act block (128-byte
+  // swizzled, for the TMA stores), GEMM2 2 KB per epilogue warp
   uint8_t* stg = stages + static_cast<size_t>(S) * kTmStageBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(stg + tm_out_bytes(MODE));
   uint64_t* empty = full + S;
@@ -289,23 +291,46 @@ __global__ void __launch_bounds__(kTmThreads, 1)
       return __all_sync(0xffffffffu, got);
     };
 
+    // Scale pointers of work item (tile, mb) for this thread's row:
+    // activation scales of the row, one per K block, and weight scales of
+    // the item's two 128-row blocks (GEMM1: the gate and the up block of the
+    // feature block; GEMM2: two consecutive output blocks).  GEMM2's second
+    // block lies past the expert's rows when H is not a multiple of 256 (its
+    // outputs are not stored): the first block's scales stand in for it
+    // rather than another expert's or those past the array.
+    auto scale_ptrs = [&](const int4& tl, int mbi, const float*& sxp, const float*& sw0p,
+                          const float*& sw1p) {
+      const int gr = tl.y + (r < tl.z ? r : 0);  // a valid row for the loads
+      sxp = P.b_scale + static_cast<size_t>(gr) * kbs;
+      sw0p = P.w_scale + (static_cast<size_t>(tl.x) * P.w_scale_rows_per_e +
+                          static_cast<size_t>(mbi) * (P.row_step / 128)) * kbs;
+      const bool blk1 = G == 0 || mbi * P.row_step + 128 < P.m_valid;
+      sw1p = blk1 ? sw0p + static_cast<size_t>(P.a_up_off / 128) * kbs : sw0p;
+    };
+    // the first item's tile and first K block's scales; later items' are
+    // loaded one item ahead (the tile) and during the previous item's last
+    // K block (the scales), off the path from one item to the next
+    int4 tile = static_cast<int>(blockIdx.x) < nwork ? P.tiles[blockIdx.x / P.mblocks]
+                                                     : int4{0, 0, 0, 0};
+    float sx_n = 0.0f, sw0_n = 0.0f, sw1_n = 0.0f;
+    if (static_cast<int>(blockIdx.x) < nwork) {
+      const float *a, *b, *c;
+      scale_ptrs(tile, blockIdx.x % P.mblocks, a, b, c);
+      sx_n = __ldg(a);
+      sw0_n = __ldg(b);
+      sw1_n = __ldg(c);
+    }
+
     for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x, ++ib) {
-      const int4 tile = P.tiles[w / P.mblocks];
+      const int wn = w + static_cast<int>(gridDim.x);
+      const int4 tile_next = wn < nwork ? P.tiles[wn / P.mblocks] : tile;
       const int mb = w % P.mblocks;
       const int row0 = tile.y, nrows = tile.z;
       const bool live = r < nrows;
-      const int grow = row0 + (live ? r : 0);  // a valid row for the scale loads
-      // activation scales of this row, one per K block; weight scales of
-      // the item's two 128-row blocks (GEMM1: the gate and the up block of
-      // the feature block; GEMM2: two consecutive output blocks)
-      const float* sxp = P.b_scale + static_cast<size_t>(grow) * kbs;
-      const float* sw0p = P.w_scale + (static_cast<size_t>(tile.x) * P.w_scale_rows_per_e +
-                                       static_cast<size_t>(mb) * (P.row_step / 128)) * kbs;
-      // GEMM2's second block lies past the expert's rows when H is not a
-      // multiple of 256 (its outputs are not stored): read the first
-      // block's scales instead of another expert's or past the array
-      const bool blk1 = G == 0 || mb * P.row_step + 128 < P.m_valid;
-      const float* sw1p = blk1 ? sw0p + static_cast<size_t>(P.a_up_off / 128) * kbs : sw0p;
+      const int grow = row0 + (live ? r : 0);
+      const float *sxp, *sw0p, *sw1p;
+      scale_ptrs(tile, mb, sxp, sw0p, sw1p);
+      tile = tile_next;
       float wt = 0.0f;  // GEMM2: the routing weight of this row's pick
       if (G == 1 && live) wt = __ldg(args.topw + __ldg(args.src + grow));
 
@@ -317,7 +342,6 @@ __global__ void __launch_bounds__(kTmThreads, 1)
         acc0[c] = make_float2(0.0f, 0.0f);
         acc1[c] = make_float2(0.0f, 0.0f);
       }
-      float sx_n = __ldg(sxp), sw0_n = __ldg(sw0p), sw1_n = __ldg(sw1p);
       for (int kb = 0; kb < kbs; ++kb, ++kc) {
         const float c0 = sx_n * sw0_n, c1 = sx_n * sw1_n;
         const float2 c02 = make_float2(c0, c0), c12 = make_float2(c1, c1);
@@ -325,6 +349,12 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           sx_n = __ldg(sxp + kb + 1);
           sw0_n = __ldg(sw0p + kb + 1);
           sw1_n = __ldg(sw1p + kb + 1);
+        } else if (wn < nwork) {  // and after the last block, the next item's first
+          const float *a, *b, *c;
+          scale_ptrs(tile_next, wn % P.mblocks, a, b, c);
+          sx_n = __ldg(a);
+          sw0_n = __ldg(b);
+          sw1_n = __ldg(c);
         }
         const uint32_t slot = kc & 1u;
         const bool got = mbar_wait(smem_u32(&accf[slot]), (kc >> 1) & 1u, limit, abort_flag);
@@ -410,37 +440,39 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           bulk_commit();
         }
       } else {
-        // weighted rows of the two output blocks, bf16, one 128-column half
-        // per round through the staging buffer
+        // weighted rows of the two output blocks, bf16.  Each warp turns its
+        // 32 rows x 32 columns of a half around in its own 2 KB of shared
+        // memory, so that every store instruction writes 8 rows x 64
+        // contiguous bytes instead of 32 rows x 16 bytes; only __syncwarp
+        // orders it.  16-byte chunk c of row l sits at chunk position
+        // c ^ ((l >> 1) & 3): both the row-wise writes and the column-wise
+        // reads then touch each bank group once per 8 lanes.
+        uint8_t* wsl = stg + ew * 2048;  // this warp's slice
         auto store_half = [&](const float2(&a)[kTmCols / 2], int half) -> bool {
-          const int h0 = mb * 256 + half * 128;  // first column of this half
-          if (h0 >= args.H) return true;         // uniform: the block past H
-          if (elected) bulk_wait_read<0>();      // the staging is free again
-          if (!ep_barrier()) return false;
-          uint8_t* box = stg + (part >> 1) * 16384;  // this thread's 64-column box
-          uint4 v[4];
+          const int h0 = mb * 256 + half * 128 + part * kTmCols;  // this warp's first column
+          if (mb * 256 + half * 128 >= args.H) return true;      // uniform: the block past H
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
-            v[i].x = pack_bf16x2(wt * a[4 * i].x, wt * a[4 * i].y);
-            v[i].y = pack_bf16x2(wt * a[4 * i + 1].x, wt * a[4 * i + 1].y);
-            v[i].z = pack_bf16x2(wt * a[4 * i + 2].x, wt * a[4 * i + 2].y);
-            v[i].w = pack_bf16x2(wt * a[4 * i + 3].x, wt * a[4 * i + 3].y);
-            *reinterpret_cast<uint4*>(box + sw128_offset(r, (part & 1) * 4 + i)) = v[i];
+            uint4 v;
+            v.x = pack_bf16x2(wt * a[4 * i].x, wt * a[4 * i].y);
+            v.y = pack_bf16x2(wt * a[4 * i + 1].x, wt * a[4 * i + 1].y);
+            v.z = pack_bf16x2(wt * a[4 * i + 2].x, wt * a[4 * i + 2].y);
+            v.w = pack_bf16x2(wt * a[4 * i + 3].x, wt * a[4 * i + 3].y);
+            *reinterpret_cast<uint4*>(wsl + lane * 64 + ((i ^ ((lane >> 1) & 3)) << 4)) = v;
           }
-          if (live && r >= n16) {  // the tile's last rows past a multiple of 16
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.ybuf) +
-                                                  static_cast<size_t>(grow) * args.H + h0 +
-                                                  part * kTmCols);
+          __syncwarp();
+          const int c = lane & 3;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) dst[i] = v[i];
+          for (int i = 0; i < 4; ++i) {
+            const int rr = i * 8 + (lane >> 2);  // row within the warp's 32
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(wsl + rr * 64 + ((c ^ ((rr >> 1) & 3)) << 4));
+            const int rt = q * 32 + rr;  // row within the tile
+            if (rt < nrows)
+              *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(args.ybuf) +
+                                        static_cast<size_t>(row0 + rt) * args.H + h0 + c * 8) = v;
           }
-          fence_proxy_async_shared();
-          if (!ep_barrier()) return false;
-          if (elected && n16 > 0) {
-            store_rows16(omaps, smem_u32(stg), n16, h0, row0);
-            store_rows16(omaps, smem_u32(stg + 16384), n16, h0 + 64, row0);
-            bulk_commit();
-          }
+          __syncwarp();
           return true;
         };
         if (!store_half(acc0, 0) || !store_half(acc1, 1)) {

@@ -124,9 +124,9 @@ cudaError_t launch_grouped_gemm_pair(int kind, int mode, const GemmArgs& args,
 
 // Token-major FP8 grouped GEMMs (grouped_gemm_tm.cu): one stage holds two
 // 128-row weight boxes and a token box of up to 128 rows (128 bytes of K
-// each).  Outside the ring: the output staging of the TMA stores (GEMM1: a
-// 128-row x 128-byte act block; GEMM2: two 128-row x 64-column bf16 boxes),
-// alignment slack, barriers and (GEMM1) the amax exchange.
+// each).  Outside the ring: output staging (GEMM1: a 128-row x 128-byte act
+// block for its TMA stores; GEMM2: 2 KB per epilogue warp to turn its rows
+// around), alignment slack, barriers and (GEMM1) the amax exchange.
 constexpr int kTmStageBytes = 3 * 16384;
 __host__ __device__ constexpr int tm_out_bytes(int mode) { return mode == 1 ? 16384 : 32768; }
 __host__ __device__ constexpr int tm_smem_bytes(int mode, int stages) {
@@ -136,8 +136,7 @@ __host__ __device__ constexpr int tm_smem_bytes(int mode, int stages) {
 // Launch token-major GEMM1 (mode 1: gate+up with SiLU and e4m3 act) or
 // GEMM2 (mode 2: down with the routing weight) over `grid` persistent CTAs.
 // `maps`: the weights (a) and the input token rows (b, 16 .. 256 rows high);
-// `omaps`: the output rows the epilogue stores with TMA (b: GEMM1 the act
-// rows, GEMM2 the y rows in 64-column boxes; 16 .. 256 rows high).
+// `omaps`: GEMM1's act rows for its TMA stores (b, 16 .. 256 rows high).
 cudaError_t launch_grouped_gemm_tm(int mode, const GemmArgs& args, const GemmMaps& maps,
                                    const GemmMaps& omaps, int grid, int smem_bytes,
                                    cudaStream_t stream);

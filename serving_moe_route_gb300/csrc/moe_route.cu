@@ -601,16 +601,15 @@ static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
 struct MapKey {
   int dev, kind, H, I, EL, pair;
   long long R;
-  const void *w13, *w2, *xq, *act, *y;
+  const void *w13, *w2, *xq, *act;
   bool operator==(const MapKey& o) const {
     return dev == o.dev && kind == o.kind && H == o.H && I == o.I && EL == o.EL &&
            pair == o.pair && R == o.R && w13 == o.w13 && w2 == o.w2 && xq == o.xq &&
-           act == o.act && y == o.y;
+           act == o.act;
   }
 };
 struct MapSet {
   GemmMaps m1, m2, h1, h2;  // h1/h2: half-height token maps (CTA pairs)
-  GemmMaps ys;              // FP8: bf16 y rows in 64-column boxes (TMA stores)
 };
 
 static bool encode_maps(const MapKey& key, MapSet* s) {
@@ -634,10 +633,6 @@ static bool encode_maps(const MapKey& key, MapSet* s) {
     ok = make_tmap(&s->h1.b[i], key.xq, dt, esize, key.H, key.R, rows) &&
          make_tmap(&s->h2.b[i], key.act, dt, esize, key.I, key.R, rows);
   }
-  s->ys = s->m2;
-  for (int i = 0; i < kTokMaps && ok && key.kind == KIND_E4M3; ++i)  // y rows, 16 .. 256 high
-    ok = make_tmap(&s->ys.b[i], key.y, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, key.H, key.R,
-                   16u << i);
   return ok;
 }
 
@@ -825,7 +820,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   const bool pair = pair_plan;
   MapSet ms;
-  if (!cached_maps(MapKey{dev, kind, H, I, EL, pair ? 1 : 0, R, w13, w2, xq, act, ybuf}, &ms))
+  if (!cached_maps(MapKey{dev, kind, H, I, EL, pair ? 1 : 0, R, w13, w2, xq, act}, &ms))
     return MOE_ERR_CUDA;
   const GemmMaps& m1 = ms.m1;
   const GemmMaps& m2 = ms.m2;
@@ -857,9 +852,9 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
       const int smem = tm_smem_bytes(mode, g.stages);
       const long long items = static_cast<long long>(p->max_tiles) * g.p[mode - 1].mblocks;
       const int grid = static_cast<int>(items < sms ? items : sms);
-      // GEMM1 reads x rows and stores act rows; GEMM2 reads act rows, stores y
-      if (launch_grouped_gemm_tm(mode, g, mode == 1 ? m1 : m2, mode == 1 ? m2 : ms.ys, grid, smem,
-                                 st) != cudaSuccess)
+      // GEMM1 reads x rows and stores act rows with TMA; GEMM2 reads act rows
+      // (its y rows go out with plain stores)
+      if (launch_grouped_gemm_tm(mode, g, mode == 1 ? m1 : m2, m2, grid, smem, st) != cudaSuccess)
         return MOE_ERR_CUDA;
       mark(3 + mode);
     }
