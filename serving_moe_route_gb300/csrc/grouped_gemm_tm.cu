@@ -215,8 +215,13 @@ __global__ void __launch_bounds__(kTmThreads, 1)
           const uint32_t fb = smem_u32(&full[s]);
           mbar_arrive_expect_tx(fb, tx);
           const int kx = kb * 128;
-          tma_load_2d(smem_u32(st), &maps.a, fb, kx, b_row, pol_w);
-          tma_load_2d(smem_u32(st + 16384), &maps.a, fb, kx, b_row + P.a_up_off, pol_w);
+          // the item's 256 weight rows in one copy: GEMM1's gate block and up
+          // block as the two planes of a 3-D box, GEMM2's two output blocks
+          // as one 256-row box
+          if constexpr (G == 0)
+            tma_load_3d(smem_u32(st), &maps.a, fb, kx, mb * 128, 2 * tile.x, pol_w);
+          else
+            tma_load_2d(smem_u32(st), &maps.a, fb, kx, b_row, pol_w);
           tma_load_2d(smem_u32(st + 32768), tmx, fb, kx, tile.y, pol_x);
         }
       }

@@ -592,6 +592,22 @@ static bool make_tmap(CUtensorMap* m, const void* base, CUtensorMapDataType dt, 
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D K-major tensor map over w13 [E, 2I, H] seen as [2E planes, I rows, H]
+// (plane 2e is expert e's gate rows, 2e+1 its up rows); box = 128 bytes x 128
+// rows x 2 planes, so one copy brings a feature block's gate and up rows
+static bool make_tmap_gate_up(CUtensorMap* m, const void* base, CUtensorMapDataType dt, int esize,
+                              uint64_t H, uint64_t I, uint64_t EL) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {H, I, 2 * EL};
+  cuuint64_t strides[2] = {H * static_cast<uint64_t>(esize), I * H * static_cast<uint64_t>(esize)};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esize), 128, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The TMA tensor maps of one forward: weights (w13, w2) and the permuted
 // token rows (xq, act) at every box height, plus the half-height token maps
 // of CTA-pair plans.  A map only encodes an address, a shape and a box, so
@@ -610,6 +626,7 @@ struct MapKey {
 };
 struct MapSet {
   GemmMaps m1, m2, h1, h2;  // h1/h2: half-height token maps (CTA pairs)
+  GemmMaps t1, t2;          // FP8 token-major: 256 weight rows per copy
 };
 
 static bool encode_maps(const MapKey& key, MapSet* s) {
@@ -633,6 +650,11 @@ static bool encode_maps(const MapKey& key, MapSet* s) {
     ok = make_tmap(&s->h1.b[i], key.xq, dt, esize, key.H, key.R, rows) &&
          make_tmap(&s->h2.b[i], key.act, dt, esize, key.I, key.R, rows);
   }
+  s->t1 = s->m1;
+  s->t2 = s->m2;
+  if (ok && key.kind == KIND_E4M3)
+    ok = make_tmap_gate_up(&s->t1.a, key.w13, dt, esize, key.H, key.I, key.EL) &&
+         make_tmap(&s->t2.a, key.w2, dt, esize, key.I, static_cast<uint64_t>(key.EL) * key.H, 256);
   return ok;
 }
 
@@ -854,7 +876,8 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
       const int grid = static_cast<int>(items < sms ? items : sms);
       // GEMM1 reads x rows and stores act rows with TMA; GEMM2 reads act rows
       // (its y rows go out with plain stores)
-      if (launch_grouped_gemm_tm(mode, g, mode == 1 ? m1 : m2, m2, grid, smem, st) != cudaSuccess)
+      if (launch_grouped_gemm_tm(mode, g, mode == 1 ? ms.t1 : ms.t2, m2, grid, smem, st) !=
+          cudaSuccess)
         return MOE_ERR_CUDA;
       mark(3 + mode);
     }
