@@ -239,36 +239,31 @@ __global__ void __launch_bounds__(kTmThreads, 1)
     if (lane == 0) {
       // M = 128 token rows, N = 256 weight rows, e4m3 x e4m3 -> f32
       const uint32_t idesc = idesc_make(KindTraits<KIND_E4M3>::fmt, 128, 256);
-      // This CTA's K blocks, item after item: block g uses TMEM slot g & 1 and
-      // stage g % S.  The waits for block g+1 (its slot drained, its stage
-      // loaded) run while block g's first three MMAs execute, so the tensor
-      // pipe is not left idle while this thread polls barriers; block g+1
-      // never depends on block g's last MMA, so the order cannot deadlock.
-      const int items = static_cast<int>(blockIdx.x) < nwork
-                            ? (nwork - static_cast<int>(blockIdx.x) + static_cast<int>(gridDim.x) -
-                               1) / static_cast<int>(gridDim.x)
-                            : 0;
-      const uint32_t total = static_cast<uint32_t>(items) * static_cast<uint32_t>(kbs);
-      auto ready = [&](uint32_t g) -> bool {
-        return mbar_wait(smem_u32(&acce[g & 1u]), ((g >> 1) & 1u) ^ 1u, limit, abort_flag) &&
-               mbar_wait(smem_u32(&full[g % S]), (g / S) & 1u, limit, abort_flag);
-      };
-      if (total > 0 && !ready(0)) ok = false;
-      for (uint32_t g = 0; g < total && ok; ++g) {
-        tc_fence_after();
-        const uint32_t slot = g & 1u;
-        const int s = static_cast<int>(g % S);
-        const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * kTmStageBytes);
-        const uint64_t bd0 = sdesc_sw128(sa);          // 256 weight rows
-        const uint64_t ad0 = sdesc_sw128(sa + 32768);  // 128 token rows
-        const uint32_t d = tmem_base + slot * 256u;
+      uint32_t it = 0, kc = 0;
+      for (int w = blockIdx.x; w < nwork && ok; w += gridDim.x) {
+        for (int kb = 0; kb < kbs; ++kb, ++it, ++kc) {
+          const uint32_t slot = kc & 1u;
+          if (!mbar_wait(smem_u32(&acce[slot]), ((kc >> 1) & 1u) ^ 1u, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int s = static_cast<int>(it % S);
+          if (!mbar_wait(smem_u32(&full[s]), (it / S) & 1u, limit, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(stages + static_cast<size_t>(s) * kTmStageBytes);
+          const uint64_t bd0 = sdesc_sw128(sa);          // 256 weight rows
+          const uint64_t ad0 = sdesc_sw128(sa + 32768);  // 128 token rows
 #pragma unroll
-        for (int ks = 0; ks < 3; ++ks)
-          mma_issue<KIND_E4M3>(d, ad0 + 2u * ks, bd0 + 2u * ks, idesc, ks != 0);
-        if (g + 1 < total && !ready(g + 1)) ok = false;  // block g still completes below
-        mma_issue<KIND_E4M3>(d, ad0 + 6u, bd0 + 6u, idesc, 1u);
-        mma_commit(smem_u32(&empty[s]));    // frees the stage once read
-        mma_commit(smem_u32(&accf[slot]));  // the K block's partial is in TMEM
+          for (int ks = 0; ks < 4; ++ks)
+            mma_issue<KIND_E4M3>(tmem_base + slot * 256u, ad0 + 2u * ks, bd0 + 2u * ks, idesc,
+                                 ks != 0);
+          mma_commit(smem_u32(&empty[s]));    // frees the stage once read
+          mma_commit(smem_u32(&accf[slot]));  // the K block's partial is in TMEM
+        }
       }
       if (!ok) {
         *abort_flag = 1;
