@@ -174,6 +174,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  if (MODE != 2 && args.spec_experts > 0 && warp == 0 && lane == 0) {
+    // The routing, scan and gather kernels are still running and HBM is
+    // mostly idle.  With one tile per expert in expert order (routing that
+    // touches every expert a few times), this CTA's first work item is
+    // likely item blockIdx.x: expert blockIdx.x / mblocks.  The weights are
+    // an input, not a predecessor's output, so its first K blocks can be
+    // brought into L2 now; a wrong guess costs only idle bandwidth.
+    const GemmPhase& P0 = args.p[0];
+    const int e = static_cast<int>(blockIdx.x) / P0.mblocks;
+    if (e < args.spec_experts) {
+      const int a_row = e * P0.a_rows_per_e + (static_cast<int>(blockIdx.x) % P0.mblocks) * P0.row_step;
+      const int nk = P0.kblocks < 16 ? P0.kblocks : 16;
+      for (int kb = 0; kb < nk; ++kb) {
+        tma_prefetch_2d(&maps1.a, kb * BKE, a_row);
+        tma_prefetch_2d(&maps1.a, kb * BKE, a_row + P0.a_up_off);
+      }
+    }
+  }
   // everything above is local set-up; the tile lists and token rows are the
   // predecessor kernels' output
   pdl_wait();

@@ -70,6 +70,11 @@ struct GemmArgs {
   int H;
   unsigned* err;
   unsigned long long limit_ns;
+  // GEMM1 weight prefetch before the predecessor kernels finish: when > 0,
+  // CTA c assumes its first work item is item c of a list that has one tile
+  // per expert in expert order (experts [0, spec_experts)), and prefetches
+  // that item's first K blocks of weights into L2 while it waits
+  int spec_experts;
 };
 
 // smem bytes for one pipeline stage: na weight tiles of 128 rows x 128 B

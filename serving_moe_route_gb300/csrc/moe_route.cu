@@ -938,6 +938,10 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
                      (H + 128 * na2 - 1) / (128 * na2), kb2, H, 128, H, s2,
                      fp8 ? H / 128 : 0, as};
   g.dep = dep;
+  // early L2 prefetch of GEMM1 weights when every expert is likely to hold
+  // one tile (est at least 4 rows and at most half the kernel's tile width)
+  const int kern_nt = fp8 ? fp8_nt : p->tile_n;
+  g.spec_experts = (p->est >= 4 && 2 * p->est <= kern_nt) ? EL : 0;
   g.R = static_cast<int>(R);
   g.act = act;
   g.act_scale = as;
