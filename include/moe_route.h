@@ -106,7 +106,10 @@ extern "C" {
  *   dep     int32 [max_tiles + 2] finished GEMM1 items per tile (when both
  *                           GEMMs run as one launch), then the work counters
  *                           of the GEMM launches
- *   err     uint32 [1]      device error word (MOE_DEVERR_* bits)
+ *   err     uint32 [1]      device error word (MOE_DEVERR_* bits); the word
+ *                           after it is internal (the call's routing breadth,
+ *                           read by the next call on the same workspace to
+ *                           decide an early weight prefetch)
  *   y       [T*k, H]        routing-weighted expert output per permuted
  *                           row (bf16; f32 for the f32 layer)
  * The remaining regions (chunk counts, permuted activations, scales) are

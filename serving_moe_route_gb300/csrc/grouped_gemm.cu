@@ -174,16 +174,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (MODE != 2 && args.spec_experts > 0 && warp == 0 && lane == 0) {
+  if (MODE != 2 && args.spec_hint && warp == 0 && lane == 0) {
     // The routing, scan and gather kernels are still running and HBM is
-    // mostly idle.  With one tile per expert in expert order (routing that
-    // touches every expert a few times), this CTA's first work item is
-    // likely item blockIdx.x: expert blockIdx.x / mblocks.  The weights are
-    // an input, not a predecessor's output, so its first K blocks can be
-    // brought into L2 now; a wrong guess costs only idle bandwidth.
+    // mostly idle.  With about one tile per expert in expert order (routing
+    // that touches nearly every expert, judged by the previous call), this
+    // CTA's first work item is likely item blockIdx.x: expert
+    // blockIdx.x / mblocks.  The weights are an input, not a predecessor's
+    // output, so its first K blocks can be brought into L2 now; a wrong
+    // guess costs only idle bandwidth.
     const GemmPhase& P0 = args.p[0];
+    const unsigned h = ld_relaxed_gpu(args.spec_hint);
+    const bool wide = (h & 0xffff0000u) == kSpecHintTag &&
+                      static_cast<int>(h & 0xffffu) >= args.spec_min;
     const int e = static_cast<int>(blockIdx.x) / P0.mblocks;
-    if (e < args.spec_experts) {
+    if (wide && e < args.spec_experts) {
       const int a_row = e * P0.a_rows_per_e + (static_cast<int>(blockIdx.x) % P0.mblocks) * P0.row_step;
       const int nk = P0.kblocks < 16 ? P0.kblocks : 16;
       for (int kb = 0; kb < nk; ++kb) {

@@ -70,12 +70,20 @@ struct GemmArgs {
   int H;
   unsigned* err;
   unsigned long long limit_ns;
-  // GEMM1 weight prefetch before the predecessor kernels finish: when > 0,
-  // CTA c assumes its first work item is item c of a list that has one tile
-  // per expert in expert order (experts [0, spec_experts)), and prefetches
-  // that item's first K blocks of weights into L2 while it waits
+  // GEMM1 weight prefetch before the predecessor kernels finish: when the
+  // word at spec_hint (written by the previous call's scan on this
+  // workspace: kSpecHintTag | experts routed to) says that call routed to at
+  // least spec_min of the spec_experts local experts, CTA c assumes its
+  // first work item is item c of a list with about one tile per expert in
+  // expert order, and prefetches that item's first K blocks of weights into
+  // L2 while it waits.  The word is read with a relaxed load (the current
+  // call's scan may be writing it); it only steers a prefetch.
   int spec_experts;
+  int spec_min;
+  const unsigned* spec_hint;
 };
+
+constexpr unsigned kSpecHintTag = 0x5ec00000u;
 
 // smem bytes for one pipeline stage: na weight tiles of 128 rows x 128 B
 // and one token tile of n_max rows x 128 B

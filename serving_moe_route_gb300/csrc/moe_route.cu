@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(1024)
                 int* __restrict__ chunk_base, int* __restrict__ counts,
                 int* __restrict__ offsets, int4* __restrict__ tiles1, int* __restrict__ ntiles1,
                 int4* __restrict__ tiles2, int* __restrict__ ntiles2, int* __restrict__ dep,
-                int heavy_first, unsigned* __restrict__ err) {
+                int heavy_first, unsigned* __restrict__ err, unsigned* __restrict__ hint) {
   __shared__ int warp_sums[32];
   pdl_trigger();
   pdl_wait();
@@ -338,6 +338,12 @@ __global__ void __launch_bounds__(1024)
   const int off = block_exclusive_scan(cnt, warp_sums, &tot_rows);
   if (e < E) offsets[e] = off;
   if (e == 0) offsets[E] = tot_rows;
+  // how many of the local experts this call routes to, for the next call's
+  // GEMM (see GemmArgs::spec_hint), tagged so that stale workspace bytes
+  // never read as a count
+  const int tch = __syncthreads_count(e < E && cnt > 0);
+  if (threadIdx.x == 0)
+    st_relaxed_gpu(hint, kSpecHintTag | static_cast<unsigned>(min(tch, 0xffff)));
   write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max1), max_tiles,
                   heavy_first, warp_sums, &tot_tiles1, tiles1, ntiles1, err);
   if (n_max2 != n_max1)
@@ -817,7 +823,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const int NM2 = tm ? 128 : pair_plan ? 256 : fp8 ? fp8_nt : (p->tile_n >= 128 ? 256 : 128);
   launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, scan_tile,
                  per_expert, NM1, NM2, p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
-                 tiles2, ntiles2, dep, pair_plan ? 1 : 0, err);
+                 tiles2, ntiles2, dep, pair_plan ? 1 : 0, err, err + 1);
   mark(2);
   // a-2 gather
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
@@ -938,10 +944,12 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
                      (H + 128 * na2 - 1) / (128 * na2), kb2, H, 128, H, s2,
                      fp8 ? H / 128 : 0, as};
   g.dep = dep;
-  // early L2 prefetch of GEMM1 weights when every expert is likely to hold
-  // one tile (est at least 4 rows and at most half the kernel's tile width)
-  const int kern_nt = fp8 ? fp8_nt : p->tile_n;
-  g.spec_experts = (p->est >= 4 && 2 * p->est <= kern_nt) ? EL : 0;
+  // early L2 prefetch of GEMM1 weights, when the previous call on this
+  // workspace routed to nearly every local expert (the tile list then has
+  // about one tile per expert, in expert order)
+  g.spec_experts = EL;
+  g.spec_min = EL - EL / 16;
+  g.spec_hint = err + 1;
   g.R = static_cast<int>(R);
   g.act = act;
   g.act_scale = as;
