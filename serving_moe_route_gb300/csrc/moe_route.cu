@@ -325,40 +325,16 @@ __global__ void __launch_bounds__(1024)
   // fused-GEMM tile counters and the two work counters that follow them
   for (int i = threadIdx.x; i < max_tiles + 2; i += blockDim.x) dep[i] = 0;
   __shared__ int tot_rows, tot_tiles1, tot_tiles2;
-  __shared__ int cnt_sm[1024];
   const int e = threadIdx.x;
-  // per-expert totals over the routing chunks and each chunk's base: G
-  // consecutive lanes per expert (G = 1024 / E rounded to a power of two,
-  // at most 32), each walking a contiguous run of chunks, their partial sums
-  // scanned across the G lanes; the sums come out in chunk order as in a
-  // single sequential pass
-  int ep = 1;
-  while (ep < E) ep <<= 1;
-  const int G = ep >= 1024 ? 1 : (1024 / ep > 32 ? 32 : 1024 / ep);
-  {
-    const int eg = threadIdx.x / G, j = threadIdx.x % G;
-    const int per = (n_chunks + G - 1) / G;
-    const int c0 = j * per, c1 = min(n_chunks, c0 + per);
-    int part = 0;
-    if (eg < E)
-      for (int c = c0; c < c1; ++c) part += chunk_counts[static_cast<size_t>(c) * E + eg];
-    int incl = part;
-    for (int off = 1; off < G; off <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, incl, off, G);
-      if (j >= off) incl += y;
+  int cnt = 0;
+  if (e < E) {
+    for (int c = 0; c < n_chunks; ++c) {
+      const size_t i = static_cast<size_t>(c) * E + e;
+      chunk_base[i] = cnt;
+      cnt += chunk_counts[i];
     }
-    int run = incl - part;
-    if (eg < E)
-      for (int c = c0; c < c1; ++c) {
-        const size_t i = static_cast<size_t>(c) * E + eg;
-        chunk_base[i] = run;
-        run += chunk_counts[i];
-      }
-    if (eg < E && j == G - 1) cnt_sm[eg] = incl;
+    counts[e] = cnt;
   }
-  __syncthreads();
-  const int cnt = e < E ? cnt_sm[e] : 0;
-  if (e < E) counts[e] = cnt;
   const int off = block_exclusive_scan(cnt, warp_sums, &tot_rows);
   if (e < E) offsets[e] = off;
   if (e == 0) offsets[E] = tot_rows;
