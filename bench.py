@@ -418,6 +418,9 @@ def gemm_roofline(wl, stage_ms, acc, pk):
     if g2 < 0.02 * g1:  # both GEMMs ran as one launch (shared tile list)
         name, ms, nbytes, flops = "gemm1+gemm2 fused", g1, acc["g1_bytes"] + acc["g2_bytes"], \
             acc["flops"]
+    elif g1 < 0.05 * g2:  # the device chose the CTA-pair family: both GEMMs in stage 2
+        name, ms, nbytes, flops = "gemm1+gemm2 (CTA pairs, chosen on the device)", g2, \
+            acc["g1_bytes"] + acc["g2_bytes"], acc["flops"]
     elif g1 >= g2:
         name, ms, nbytes, flops = "gemm1", g1, acc["g1_bytes"], acc["flops"] * 2.0 / 3.0
     else:

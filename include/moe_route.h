@@ -106,10 +106,12 @@ extern "C" {
  *   dep     int32 [max_tiles + 2] finished GEMM1 items per tile (when both
  *                           GEMMs run as one launch), then the work counters
  *                           of the GEMM launches
- *   err     uint32 [1]      device error word (MOE_DEVERR_* bits); the word
- *                           after it is internal (the call's routing breadth,
- *                           read by the next call on the same workspace to
- *                           decide an early weight prefetch)
+ *   err     uint32 [1]      device error word (MOE_DEVERR_* bits); the two
+ *                           words after it are internal: the call's routing
+ *                           breadth (read by the next call on the same
+ *                           workspace to decide an early weight prefetch),
+ *                           and the GEMM kernel family the call chose (1 one
+ *                           CTA per tile, 2 CTA pairs; see gemm_pair)
  *   y       [T*k, H]        routing-weighted expert output per permuted
  *                           row (bf16; f32 for the f32 layer)
  * The remaining regions (chunk counts, permuted activations, scales) are
@@ -140,9 +142,12 @@ typedef struct moe_plan {
   int32_t topk_group; /* groups kept per token */
   int32_t gemm_pair;  /* 1: the grouped GEMMs run on CTA pairs (cta_group::2,
                          BF16/F32 with est > 32): token tiles up to 256 rows,
-                         items of 256 weight rows; 0: one CTA per tile.  Set by
-                         moe_plan; a caller may clear or set it (ignored for
-                         FP8). */
+                         items of 256 weight rows; 0: one CTA per tile -- for
+                         BF16/F32 plans with est <= 32 and T >= 256 the device
+                         then still picks CTA pairs for a call in which an
+                         expert holds 256 rows or more (concentrated
+                         routing).  Set by moe_plan; a caller may clear or
+                         set it (ignored for FP8). */
   int32_t gemm_tm;    /* FP8 only.  1: token-major grouped GEMMs -- every
                          expert's rows in tiles of 128 on the MMA's M side,
                          256 weight rows on its N side (gate and up rows of a
@@ -228,8 +233,10 @@ int moe_forward(const moe_plan_t* plan, const void* x, const void* logits, const
  * routing kernel, [1] after routing, [2] after the scan, [3] after the
  * gather, [4] after grouped GEMM 1, [5] after grouped GEMM 2, [6] after the
  * combine.  When both GEMMs run as one launch, [4] follows that launch and
- * [5] directly follows [4].  n_events must be 7.  Same arguments, errors and
- * results as moe_forward otherwise.
+ * [5] directly follows [4].  When the device chooses the kernel family (see
+ * gemm_pair), [4] follows the one-CTA-per-tile launch and [5] the CTA-pair
+ * launches; the family not chosen finds no work.  n_events must be 7.  Same
+ * arguments, errors and results as moe_forward otherwise.
  */
 int moe_forward_timed(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,
                       const float* s13, const void* w2, const float* s2, void* out, void* ws,

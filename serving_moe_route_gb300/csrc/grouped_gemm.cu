@@ -200,8 +200,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // predecessor kernels' output
   pdl_wait();
 
-  const int nwork1 = args.run1 ? (*args.p[0].ntiles) * args.p[0].mblocks : 0;
-  const int nwork2 = args.run2 ? (*args.p[1].ntiles) * args.p[1].mblocks : 0;
+  // a device-chosen kernel family that is not this one: no work
+  const bool chosen = !args.family || *args.family == args.family_want;
+  const int nwork1 = (chosen && args.run1) ? (*args.p[0].ntiles) * args.p[0].mblocks : 0;
+  const int nwork2 = (chosen && args.run2) ? (*args.p[1].ntiles) * args.p[1].mblocks : 0;
   const int nwork = nwork1 + nwork2;
   int never = 0;
   bool ok = true;

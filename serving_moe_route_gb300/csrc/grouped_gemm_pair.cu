@@ -125,7 +125,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   pdl_wait();  // the tile list and token rows are the predecessor kernels' output
 
-  const int nwork = (*P.ntiles) * P.mblocks;
+  // a device-chosen kernel family that is not this one: no work
+  const bool chosen = !args.family || *args.family == args.family_want;
+  const int nwork = chosen ? (*P.ntiles) * P.mblocks : 0;
   int never = 0;
   bool ok = true;
 

@@ -81,7 +81,17 @@ struct GemmArgs {
   int spec_experts;
   int spec_min;
   const unsigned* spec_hint;
+  // Kernel family chosen on the device: when family is set, this launch
+  // runs only if *family == family_want (written by this call's scan kernel,
+  // read after the dependent-launch wait); otherwise it has no work.
+  const unsigned* family;
+  unsigned family_want;
 };
+
+// family words written by the scan kernel of plans that choose the GEMM
+// kernel family on the device
+constexpr unsigned kFamilySingle = 1u;  // one CTA per tile (moe_gemm_kernel)
+constexpr unsigned kFamilyPair = 2u;    // CTA pairs (moe_gemm_pair_kernel)
 
 constexpr unsigned kSpecHintTag = 0x5ec00000u;
 

@@ -40,6 +40,7 @@ constexpr int kMaxK = 32;
 constexpr int kMaxE = 1024;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s per pipeline wait
 constexpr int kTmMinEst = 32;  // FP8 plans from this estimate on run token-major
+constexpr int kHotRows = 256;  // rows of an expert that select CTA pairs on the device
 
 // ------------------------------------------------------------------ routing
 __device__ __forceinline__ float sanitize_logit(float v) {
@@ -318,7 +319,8 @@ __global__ void __launch_bounds__(1024)
                 int* __restrict__ chunk_base, int* __restrict__ counts,
                 int* __restrict__ offsets, int4* __restrict__ tiles1, int* __restrict__ ntiles1,
                 int4* __restrict__ tiles2, int* __restrict__ ntiles2, int* __restrict__ dep,
-                int heavy_first, unsigned* __restrict__ err, unsigned* __restrict__ hint) {
+                int heavy_first, unsigned* __restrict__ err, unsigned* __restrict__ hint,
+                int hot_rows, unsigned* __restrict__ family) {
   __shared__ int warp_sums[32];
   pdl_trigger();
   pdl_wait();
@@ -344,6 +346,19 @@ __global__ void __launch_bounds__(1024)
   const int tch = __syncthreads_count(e < E && cnt > 0);
   if (threadIdx.x == 0)
     st_relaxed_gpu(hint, kSpecHintTag | static_cast<unsigned>(min(tch, 0xffff)));
+  // Plans that choose the GEMM kernel family here (hot_rows > 0): an expert
+  // with at least hot_rows rows (a whole 256-row CTA-pair tile) selects the
+  // CTA-pair kernels and their tile list (widths up to 256, heavy experts
+  // first); otherwise the single-CTA list the host asked for.  Concentrated
+  // routing (H20 article, paras. 4 and 6) is the case this serves.
+  if (hot_rows > 0) {
+    const bool hot = __syncthreads_or(e < E && cnt >= hot_rows) != 0;
+    if (threadIdx.x == 0) *family = hot ? kFamilyPair : kFamilySingle;
+    if (hot) {
+      n_max1 = n_max2 = 256;
+      heavy_first = 1;
+    }
+  }
   write_tile_list(e, E, cnt, off, expert_tile(cnt, tile_n, per_expert, n_max1), max_tiles,
                   heavy_first, warp_sums, &tot_tiles1, tiles1, ntiles1, err);
   if (n_max2 != n_max1)
@@ -821,9 +836,15 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const bool pair_plan = p->gemm_pair != 0 && !fp8;
   const int NM1 = tm ? 128 : pair_plan ? 256 : fp8 ? fp8_nt : 128;
   const int NM2 = tm ? 128 : pair_plan ? 256 : fp8 ? fp8_nt : (p->tile_n >= 128 ? 256 : 128);
+  // BF16/F32 plans that run one CTA per tile and one fused launch, with
+  // enough tokens for an expert to fill a 256-row CTA-pair tile, choose the
+  // kernel family on the device, from the rows the experts actually hold
+  const bool dyn = !fp8 && !pair_plan && p->est <= 32 && NM1 == NM2 && T >= kHotRows;
+  unsigned* family = err + 2;
   launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, scan_tile,
                  per_expert, NM1, NM2, p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
-                 tiles2, ntiles2, dep, pair_plan ? 1 : 0, err, err + 1);
+                 tiles2, ntiles2, dep, pair_plan ? 1 : 0, err, err + 1, dyn ? kHotRows : 0,
+                 family);
   mark(2);
   // a-2 gather
   const long long gwarps = static_cast<long long>(T) * ((H + 255) / 256);
@@ -846,7 +867,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   const int esize = kind == KIND_TF32 ? 4 : kind == KIND_BF16 ? 2 : 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-  const bool pair = pair_plan;
+  const bool pair = pair_plan || dyn;  // the CTA-pair maps are needed
   MapSet ms;
   if (!cached_maps(MapKey{dev, kind, H, I, EL, pair ? 1 : 0, R, w13, w2, xq, act}, &ms))
     return MOE_ERR_CUDA;
@@ -887,106 +908,132 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
         return MOE_ERR_CUDA;
       mark(3 + mode);
     }
-  } else if (pair) {
-    // CTA pairs: half-height token maps, items of 256 weight rows, one
-    // token tile list (widths up to 256) for both GEMMs
-    const GemmMaps& h1 = ms.h1;
-    const GemmMaps& h2 = ms.h2;
-    GemmArgs g{};
-    g.p[0] = GemmPhase{tiles, ntiles, 2, 256, (I + 255) / 256, kb1, 2 * I, I, I, nullptr, 0,
-                       nullptr};
-    g.p[1] = GemmPhase{tiles, ntiles, 1, 256, (H + 255) / 256, kb2, H, 128, H, nullptr, 0,
-                       nullptr};
-    g.R = static_cast<int>(R);
-    g.act = act;
-    g.I = I;
-    g.src = src;
-    g.topw = topw;
-    g.ybuf = ybuf;
-    g.H = H;
-    g.err = err;
-    g.limit_ns = kWaitLimitNs;
-    g.n_max = 256;
-    auto launch_pair = [&](int mode, const GemmMaps& maps) -> bool {
-      const int na = mode == 1 ? 2 : 1;
-      g.run1 = mode == 1;
-      g.run2 = mode == 2;
-      g.na_max = na;
-      const int budget = 227 * 1024 - kPairExtraSmem;
-      const int sb = gemm_pair_stage_bytes(na, g.n_max, mode == 1 ? 1 : 2);
-      g.stages = budget / sb > 8 ? 8 : budget / sb;
-      g.nslots = 512 / (na * g.n_max) >= 2 ? 2 : 1;
-      g.tmem_cols = 512;
-      const int smem = g.stages * sb + kPairExtraSmem;
-      const long long items = static_cast<long long>(p->max_tiles) * g.p[mode - 1].mblocks;
-      return launch_grouped_gemm_pair(kind, mode, g, maps, smem, items, st) == cudaSuccess;
+  } else {
+    // CTA-pair launches (GEMM1 then GEMM2) and single-CTA launches (one
+    // fused, or GEMM1 then GEMM2); `want` non-zero: the launch runs only if
+    // this call's scan chose that family; `marks`: record the GEMM events
+    auto run_pair = [&](unsigned want, bool marks) -> bool {
+      // CTA pairs: half-height token maps, items of 256 weight rows, one
+      // token tile list (widths up to 256) for both GEMMs
+      const GemmMaps& h1 = ms.h1;
+      const GemmMaps& h2 = ms.h2;
+      GemmArgs g{};
+      g.p[0] = GemmPhase{tiles, ntiles, 2, 256, (I + 255) / 256, kb1, 2 * I, I, I, nullptr, 0,
+                         nullptr};
+      g.p[1] = GemmPhase{tiles, ntiles, 1, 256, (H + 255) / 256, kb2, H, 128, H, nullptr, 0,
+                         nullptr};
+      g.R = static_cast<int>(R);
+      g.act = act;
+      g.I = I;
+      g.src = src;
+      g.topw = topw;
+      g.ybuf = ybuf;
+      g.H = H;
+      g.err = err;
+      g.limit_ns = kWaitLimitNs;
+      g.family = want ? family : nullptr;
+      g.family_want = want;
+      g.n_max = 256;
+      auto launch_pair = [&](int mode, const GemmMaps& maps) -> bool {
+        const int na = mode == 1 ? 2 : 1;
+        g.run1 = mode == 1;
+        g.run2 = mode == 2;
+        g.na_max = na;
+        const int budget = 227 * 1024 - kPairExtraSmem;
+        const int sb = gemm_pair_stage_bytes(na, g.n_max, mode == 1 ? 1 : 2);
+        g.stages = budget / sb > 8 ? 8 : budget / sb;
+        g.nslots = 512 / (na * g.n_max) >= 2 ? 2 : 1;
+        g.tmem_cols = 512;
+        const int smem = g.stages * sb + kPairExtraSmem;
+        const long long items = static_cast<long long>(p->max_tiles) * g.p[mode - 1].mblocks;
+        return launch_grouped_gemm_pair(kind, mode, g, maps, smem, items, st) == cudaSuccess;
+      };
+      if (!launch_pair(1, h1)) return false;
+      if (marks) mark(4);
+      if (!launch_pair(2, h2)) return false;
+      if (marks) mark(5);
+      return true;
     };
-    if (!launch_pair(1, h1)) return MOE_ERR_CUDA;
-    mark(4);
-    if (!launch_pair(2, h2)) return MOE_ERR_CUDA;
-    mark(5);
-  } else {
-  GemmArgs g{};
-  g.p[0] = GemmPhase{tiles, ntiles, 2, 128, p->g1_mblocks, kb1, 2 * I, I, I, s13,
-                     fp8 ? 2 * I / 128 : 0, xs};
-  // one launch for both GEMMs when they share a tile list and experts hold
-  // few rows (est <= 32): GEMM2 work then fills the tail of GEMM1's.  With
-  // more rows per expert GEMM1's items are many and short relative to the
-  // whole, and two launches with their own stage layouts run faster.
-  const bool fused = NM1 == NM2 && p->est <= 32;
-  // fused GEMM2 items take two 128-row weight tiles (256 output rows), so
-  // that they stream as many weight bytes per stage as GEMM1 items; FP8
-  // GEMM2 items do so as well, halving the per-item epilogue work (scale
-  // staging, barriers) per output row
-  const int na2 = ((fused || fp8) && H % 256 == 0) ? 2 : 1;
-  const bool one_list = NM1 == NM2;  // the scan writes list 2 only when widths differ
-  g.p[1] = GemmPhase{one_list ? tiles : tiles2, one_list ? ntiles : ntiles2, na2, 128 * na2,
-                     (H + 128 * na2 - 1) / (128 * na2), kb2, H, 128, H, s2,
-                     fp8 ? H / 128 : 0, as};
-  g.dep = dep;
-  // early L2 prefetch of GEMM1 weights, when the previous call on this
-  // workspace routed to nearly every local expert (the tile list then has
-  // about one tile per expert, in expert order)
-  g.spec_experts = EL;
-  g.spec_min = EL - EL / 16;
-  g.spec_hint = err + 1;
-  g.R = static_cast<int>(R);
-  g.act = act;
-  g.act_scale = as;
-  g.I = I;
-  g.src = src;
-  g.topw = topw;
-  g.ybuf = ybuf;
-  g.H = H;
-  g.err = err;
-  g.limit_ns = kWaitLimitNs;
-  const GemmMaps maps[2] = {m1, m2};
-  auto launch = [&](int run1, int run2, int nm, int na) -> bool {
-    g.work_counter = dep + p->max_tiles + (run1 ? 0 : 1);  // zeroed by the scan
-    g.run1 = run1;
-    g.run2 = run2;
-    g.fused = run1 && run2;
-    g.n_max = nm;
-    g.na_max = na;
-    g.stages = max_stages(na, nm, kbmax, fp8);
-    g.nslots = slots_for(na, nm, fp8);
-    g.tmem_cols = tmem_cols_for(g.nslots * na * nm);
-    const long long work = static_cast<long long>(p->max_tiles) *
-                           ((run1 ? g.p[0].mblocks : 0) + (run2 ? g.p[1].mblocks : 0));
-    const int grid = static_cast<int>(work < sms ? work : sms);
-    const int smem = g.stages * gemm_stage_bytes(na, nm) + gemm_extra_smem(nm, kbmax, fp8);
-    return launch_grouped_gemm(kind, g, maps, grid, smem, st) == cudaSuccess;
-  };
-  if (fused) {
-    if (!launch(1, 1, NM1, 2)) return MOE_ERR_CUDA;
-    mark(4);
-    mark(5);
-  } else {
-    if (!launch(1, 0, NM1, 2)) return MOE_ERR_CUDA;
-    mark(4);
-    if (!launch(0, 1, NM2, na2)) return MOE_ERR_CUDA;
-    mark(5);
-  }
+    auto run_single = [&](unsigned want, bool marks) -> bool {
+      GemmArgs g{};
+      g.p[0] = GemmPhase{tiles, ntiles, 2, 128, p->g1_mblocks, kb1, 2 * I, I, I, s13,
+                         fp8 ? 2 * I / 128 : 0, xs};
+      // one launch for both GEMMs when they share a tile list and experts hold
+      // few rows (est <= 32): GEMM2 work then fills the tail of GEMM1's.  With
+      // more rows per expert GEMM1's items are many and short relative to the
+      // whole, and two launches with their own stage layouts run faster.
+      const bool fused = NM1 == NM2 && p->est <= 32;
+      // fused GEMM2 items take two 128-row weight tiles (256 output rows), so
+      // that they stream as many weight bytes per stage as GEMM1 items; FP8
+      // GEMM2 items do so as well, halving the per-item epilogue work (scale
+      // staging, barriers) per output row
+      const int na2 = ((fused || fp8) && H % 256 == 0) ? 2 : 1;
+      const bool one_list = NM1 == NM2;  // the scan writes list 2 only when widths differ
+      g.p[1] = GemmPhase{one_list ? tiles : tiles2, one_list ? ntiles : ntiles2, na2, 128 * na2,
+                         (H + 128 * na2 - 1) / (128 * na2), kb2, H, 128, H, s2,
+                         fp8 ? H / 128 : 0, as};
+      g.dep = dep;
+      // early L2 prefetch of GEMM1 weights, when the previous call on this
+      // workspace routed to nearly every local expert (the tile list then has
+      // about one tile per expert, in expert order)
+      g.spec_experts = EL;
+      g.spec_min = EL - EL / 16;
+      g.spec_hint = err + 1;
+      g.R = static_cast<int>(R);
+      g.act = act;
+      g.act_scale = as;
+      g.I = I;
+      g.src = src;
+      g.topw = topw;
+      g.ybuf = ybuf;
+      g.H = H;
+      g.err = err;
+      g.limit_ns = kWaitLimitNs;
+      g.family = want ? family : nullptr;
+      g.family_want = want;
+      const GemmMaps maps[2] = {m1, m2};
+      auto launch = [&](int run1, int run2, int nm, int na) -> bool {
+        g.work_counter = dep + p->max_tiles + (run1 ? 0 : 1);  // zeroed by the scan
+        g.run1 = run1;
+        g.run2 = run2;
+        g.fused = run1 && run2;
+        g.n_max = nm;
+        g.na_max = na;
+        g.stages = max_stages(na, nm, kbmax, fp8);
+        g.nslots = slots_for(na, nm, fp8);
+        g.tmem_cols = tmem_cols_for(g.nslots * na * nm);
+        const long long work = static_cast<long long>(p->max_tiles) *
+                               ((run1 ? g.p[0].mblocks : 0) + (run2 ? g.p[1].mblocks : 0));
+        const int grid = static_cast<int>(work < sms ? work : sms);
+        const int smem = g.stages * gemm_stage_bytes(na, nm) + gemm_extra_smem(nm, kbmax, fp8);
+        return launch_grouped_gemm(kind, g, maps, grid, smem, st) == cudaSuccess;
+      };
+      if (fused) {
+        if (!launch(1, 1, NM1, 2)) return false;
+        if (marks) {
+          mark(4);
+          mark(5);
+        }
+      } else {
+        if (!launch(1, 0, NM1, 2)) return false;
+        if (marks) mark(4);
+        if (!launch(0, 1, NM2, na2)) return false;
+        if (marks) mark(5);
+      }
+      return true;
+    };
+    if (dyn) {
+      // both families are enqueued; the one the scan did not choose finds
+      // no work.  Events: [4] after the single-CTA launch, [5] after the pair
+      if (!run_single(kFamilySingle, false)) return MOE_ERR_CUDA;
+      mark(4);
+      if (!run_pair(kFamilyPair, false)) return MOE_ERR_CUDA;
+      mark(5);
+    } else if (pair) {
+      if (!run_pair(0, true)) return MOE_ERR_CUDA;
+    } else {
+      if (!run_single(0, true)) return MOE_ERR_CUDA;
+    }
   }
 
   // a-7: sum of each token's k weighted rows

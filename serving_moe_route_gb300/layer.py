@@ -143,6 +143,9 @@ class MoELayer:
             "ntiles": view(p.off_ntiles, 1, torch.int32),
             "tiles2": view(p.off_tiles2, p.max_tiles * 4, torch.int32).view(p.max_tiles, 4),
             "ntiles2": view(p.off_ntiles2, 1, torch.int32),
+            # the GEMM kernel family a plan that chooses it on the device ran
+            # (1 one CTA per tile, 2 CTA pairs; left as it was otherwise)
+            "family": view(p.off_err + 8, 1, torch.int32),
         }
         if self.dtype == FP8:
             out["xq"] = view(p.off_xq, R * self.H, torch.uint8).view(R, self.H)

@@ -64,6 +64,11 @@ def run_gpu(wl, inp, layer=None):
     inter["tile_n"] = layer.plan(wl.T).tile_n
     inter["gemm_pair"] = layer.plan(wl.T).gemm_pair
     inter["gemm_tm"] = layer.plan(wl.T).gemm_tm
+    # plans that pick the GEMM kernel family on the device (BF16/F32, est <= 32,
+    # T >= 256): an expert with 256 or more rows selects CTA pairs
+    plan = layer.plan(wl.T)
+    inter["dyn_family"] = (wl.dtype != W.FP8 and not plan.gemm_pair and plan.est <= 32
+                           and wl.T >= 256)
     inter["est"] = layer.plan(wl.T).est
     return out.float().cpu().double().numpy(), inter, layer
 
@@ -117,7 +122,11 @@ def check_routing_and_permutation(wl, inp, inter):
     est = int(inter["est"])
     fp8_nt = 2 * tile_n if (2 * est > tile_n and tile_n < 64) else tile_n
     tm = wl.dtype == W.FP8 and int(inter["gemm_tm"])
-    if int(inter["gemm_pair"]) and wl.dtype != W.FP8:
+    if inter.get("dyn_family"):
+        hot = int(counts.max()) >= 256 if counts.size else False
+        assert int(inter["family"][0]) == (2 if hot else 1), (inter["family"], counts.max())
+    if (int(inter["gemm_pair"]) or (inter.get("dyn_family") and int(inter["family"][0]) == 2)) \
+            and wl.dtype != W.FP8:
         lists = [("tiles", "ntiles", 256)]
     elif tm:  # token-major FP8: every expert's rows in tiles of 128
         lists = [("tiles", "ntiles", 128)]

@@ -79,6 +79,14 @@ EDGE = [
              scoring=W.SIGMOID),
     W.custom("swap_ab_large_fp8", T=700, H=256, I=384, E=8, k=2, dtype=W.FP8, seed=65,
              gemm_tm=0),
+    # the kernel family chosen on the device (BF16, est <= 32, T >= 256): hot
+    # experts (>= 256 rows) select CTA pairs, uniform routing one CTA per tile
+    # (concentrated: ~90% of the picks on 6 experts, so each holds ~T*k*0.15 rows)
+    W.custom("family_pair", T=520, H=256, I=256, E=128, k=4, dtype=W.BF16, seed=68,
+             logits="concentrated"),
+    W.custom("family_single", T=300, H=256, I=256, E=64, k=4, dtype=W.BF16, seed=69),
+    W.custom("family_pair_f32", T=1000, H=128, I=96, E=128, k=2, dtype=W.F32, seed=71,
+             logits="concentrated"),
 ]
 
 
