@@ -388,6 +388,13 @@ class Runner:
     def counts(self):
         return self.layer.intermediates(self.wl.T)["counts"].cpu().tolist()
 
+    def family(self):
+        """The GEMM kernel family the last call picked on the device (1 one
+        CTA per tile, 2 CTA pairs), or None for plans that fix it."""
+        if not self.plan.gemm_dyn:
+            return None
+        return int(self.layer.intermediates(self.wl.T)["family"][0])
+
 
 def job_throughput(local_seconds, units_per_rank, device=None):
     """Whole-job throughput of independent replicas: every rank processed
@@ -409,18 +416,28 @@ def pct(v, q):
     return s[min(len(s) - 1, max(0, int(round(q * (len(s) - 1)))))]
 
 
-def gemm_roofline(wl, stage_ms, acc, pk):
+def gemm_roofline(wl, stage_ms, acc, pk, family=None, plan=None):
     """The dominant kernel (the GEMM with the larger mean time) against the
-    measured HBM copy bandwidth (decode-sized batches) or bf16 tensor peak."""
+    measured HBM copy bandwidth (decode-sized batches) or bf16 tensor peak.
+    family: the kernel family a per-call plan picked (stage 'gemm1' then
+    spans the single-CTA launch, 'gemm2' the CTA-pair ones), else None.
+    plan: the layer's plan, which names the kernel."""
     from serving_moe_route_gb300 import workloads as W
+    kern = "moe_gemm_kernel"
+    if plan is not None and wl.dtype == W.FP8 and plan.gemm_tm:
+        kern = "moe_gemm_tm_kernel"
+    elif plan is not None and wl.dtype != W.FP8 and (plan.gemm_pair or family == 2):
+        kern = "moe_gemm_pair_kernel"
     g1 = statistics.mean(stage_ms["gemm1"])
     g2 = statistics.mean(stage_ms["gemm2"])
-    if g2 < 0.02 * g1:  # both GEMMs ran as one launch (shared tile list)
-        name, ms, nbytes, flops = "gemm1+gemm2 fused", g1, acc["g1_bytes"] + acc["g2_bytes"], \
+    both = acc["g1_bytes"] + acc["g2_bytes"]
+    if family == 2:
+        name, ms, nbytes, flops = "gemm1+gemm2 on CTA pairs (picked per call)", g2, both, \
             acc["flops"]
-    elif g1 < 0.05 * g2:  # the device chose the CTA-pair family: both GEMMs in stage 2
-        name, ms, nbytes, flops = "gemm1+gemm2 (CTA pairs, chosen on the device)", g2, \
-            acc["g1_bytes"] + acc["g2_bytes"], acc["flops"]
+    elif family == 1:
+        name, ms, nbytes, flops = "gemm1+gemm2 fused (picked per call)", g1, both, acc["flops"]
+    elif g2 < 0.02 * g1:  # both GEMMs ran as one launch (shared tile list)
+        name, ms, nbytes, flops = "gemm1+gemm2 fused", g1, both, acc["flops"]
     elif g1 >= g2:
         name, ms, nbytes, flops = "gemm1", g1, acc["g1_bytes"], acc["flops"] * 2.0 / 3.0
     else:
@@ -432,13 +449,13 @@ def gemm_roofline(wl, stage_ms, acc, pk):
         achieved = nbytes / (ms * 1e-3) / 1e9
         return name, {"bound": "hbm", "achieved": round(achieved, 1), "peak": pk["hbm_gbs"],
                       "unit": "GB/s", "frac": round(achieved / pk["hbm_gbs"], 4),
-                      "traffic": None, "kernel": f"moe_gemm_kernel ({name})",
+                      "traffic": None, "kernel": f"{kern} ({name})",
                       "algorithmic_bytes": int(nbytes), "mean_ms": round(ms, 5),
                       "peak_source": pk["source"]}
     achieved = flops / (ms * 1e-3) / 1e12
     return name, {"bound": "tensor", "achieved": round(achieved, 1), "peak": tensor_pk,
                   "unit": "TFLOP/s", "frac": round(achieved / tensor_pk, 4), "traffic": None,
-                  "kernel": f"moe_gemm_kernel ({name})", "algorithmic_flops": flops,
+                  "kernel": f"{kern} ({name})", "algorithmic_flops": flops,
                   "mean_ms": round(ms, 5), "peak_source": tensor_src}
 
 
@@ -586,7 +603,7 @@ def sweep(dev, samples, pk, only=()):
         st = r.run_stages(samples)
         acc = algorithmic(wl, r.counts())
         med = statistics.median(steps)
-        gname, groof = gemm_roofline(wl, st, acc, pk)
+        gname, groof = gemm_roofline(wl, st, acc, pk, r.family(), r.plan)
         rows.append({
             "workload": name, "T": wl.T, "E": wl.E, "k": wl.k, "dtype": W.DTYPE_NAMES[wl.dtype],
             "scoring": "sigmoid" if wl.scoring else "softmax", "est_tile": [r.plan.est,
@@ -664,12 +681,14 @@ def run_ours(args):
     e2e_val, _ = job_throughput(sum(e2e_ms) * 1e-3, e2e_steps * wl.T, dev)
 
     acc = algorithmic(wl, r.counts())
-    gname, groof = gemm_roofline(wl, st, acc, pk)
+    gname, groof = gemm_roofline(wl, st, acc, pk, r.family(), r.plan)
     groof["traffic"] = ncu_traffic(wl.name)
     groof["traffic_source"] = ("profiles/ncu_traffic.json (ncu --set full, same kernel sources)"
                                if groof["traffic"] is not None else None)
     fused = statistics.mean(st["gemm2"]) < 0.02 * statistics.mean(st["gemm1"])
-    launches_per_step = 5 if fused else 6
+    # route, scan, gather, the GEMM launch(es), combine; a per-call plan
+    # queues both families (two CTA-pair launches and one single-CTA launch)
+    launches_per_step = 7 if r.plan.gemm_dyn else 5 if fused else 6
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
         "steps": steps, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),

@@ -55,7 +55,7 @@
 extern "C" {
 #endif
 
-#define MOE_ABI_VERSION 3
+#define MOE_ABI_VERSION 4
 
 /* return codes */
 #define MOE_OK 0
@@ -111,7 +111,7 @@ extern "C" {
  *                           breadth (read by the next call on the same
  *                           workspace to decide an early weight prefetch),
  *                           and the GEMM kernel family the call chose (1 one
- *                           CTA per tile, 2 CTA pairs; see gemm_pair)
+ *                           CTA per tile, 2 CTA pairs; see gemm_dyn)
  *   y       [T*k, H]        routing-weighted expert output per permuted
  *                           row (bf16; f32 for the f32 layer)
  * The remaining regions (chunk counts, permuted activations, scales) are
@@ -142,12 +142,9 @@ typedef struct moe_plan {
   int32_t topk_group; /* groups kept per token */
   int32_t gemm_pair;  /* 1: the grouped GEMMs run on CTA pairs (cta_group::2,
                          BF16/F32 with est > 32): token tiles up to 256 rows,
-                         items of 256 weight rows; 0: one CTA per tile -- for
-                         BF16/F32 plans with est <= 32 and T >= 256 the device
-                         then still picks CTA pairs for a call in which an
-                         expert holds 256 rows or more (concentrated
-                         routing).  Set by moe_plan; a caller may clear or
-                         set it (ignored for FP8). */
+                         items of 256 weight rows; 0: one CTA per tile (but
+                         see gemm_dyn).  Set by moe_plan; a caller may clear
+                         or set it (ignored for FP8). */
   int32_t gemm_tm;    /* FP8 only.  1: token-major grouped GEMMs -- every
                          expert's rows in tiles of 128 on the MMA's M side,
                          256 weight rows on its N side (gate and up rows of a
@@ -155,6 +152,15 @@ typedef struct moe_plan {
                          w2 for GEMM 2); 0: weight rows on the M side and
                          token tiles of tile_n.  Set by moe_plan when
                          est >= 32; a caller may clear or set it. */
+  int32_t gemm_dyn;   /* BF16/F32 plans with gemm_pair 0.  1: the device picks
+                         the kernel family per call -- CTA pairs when an
+                         expert holds 256 rows or more (concentrated routing,
+                         which the estimate does not foresee), one CTA per
+                         tile otherwise; both families' launches are queued
+                         and those of the family not picked return at once.
+                         Set by moe_plan when est <= 32 and T >= 256; a
+                         caller may clear it (setting it on another plan has
+                         no effect). */
   uint64_t workspace_bytes;
   uint64_t off_err, off_ids, off_w, off_chunk_counts, off_lrank, off_counts, off_offsets;
   uint64_t off_chunk_base, off_src, off_pos, off_tiles, off_ntiles;
@@ -234,8 +240,8 @@ int moe_forward(const moe_plan_t* plan, const void* x, const void* logits, const
  * gather, [4] after grouped GEMM 1, [5] after grouped GEMM 2, [6] after the
  * combine.  When both GEMMs run as one launch, [4] follows that launch and
  * [5] directly follows [4].  When the device chooses the kernel family (see
- * gemm_pair), [4] follows the one-CTA-per-tile launch and [5] the CTA-pair
- * launches; the family not chosen finds no work.  n_events must be 7.  Same
+ * gemm_dyn), [4] follows the one-CTA-per-tile launch and [5] the CTA-pair
+ * launches; the launches of the family not chosen do no work.  n_events must be 7.  Same
  * arguments, errors and results as moe_forward otherwise.
  */
 int moe_forward_timed(const moe_plan_t* plan, const void* x, const void* logits, const void* w13,

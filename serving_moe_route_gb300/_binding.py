@@ -39,7 +39,7 @@ class MoePlan(ctypes.Structure):
     _fields_ = [(n, c_i32) for n in (
         "abi_version", "T", "H", "I", "E", "k", "dtype", "scoring", "renorm", "est", "force_est",
         "tile_n", "route_tpc", "n_chunks", "max_tiles", "g1_mblocks", "g2_mblocks", "ep_size",
-        "ep_rank", "e_local", "n_group", "topk_group", "gemm_pair", "gemm_tm")]
+        "ep_rank", "e_local", "n_group", "topk_group", "gemm_pair", "gemm_tm", "gemm_dyn")]
     _fields_ += [(n, c_u64) for n in (
         "workspace_bytes", "off_err", "off_ids", "off_w", "off_chunk_counts", "off_lrank",
         "off_counts", "off_offsets", "off_chunk_base", "off_src", "off_pos", "off_tiles",
@@ -115,7 +115,7 @@ def lib() -> ctypes.CDLL:
     L.moe_ep_pack.restype = i
     L.moe_ep_combine.argtypes = [P, P, i, i, i, P, P]
     L.moe_ep_combine.restype = i
-    if L.moe_abi_version() != 3:
+    if L.moe_abi_version() != 4:
         raise RuntimeError("libmoe_route ABI version mismatch")
     _lib = L
     return L

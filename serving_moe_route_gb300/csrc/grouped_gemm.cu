@@ -137,6 +137,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* red = cs + 2 * kb_max * NM;
 
   pdl_trigger();
+  auto early_prefetch = [&]() {
+    if (MODE == 2 || !args.spec_hint || warp != 0 || lane != 0) return;
+    // The routing, scan and gather kernels are still running and HBM is
+    // mostly idle.  With about one tile per expert in expert order (routing
+    // that touches nearly every expert, judged by the previous call), this
+    // CTA's first work item is likely item blockIdx.x: expert
+    // blockIdx.x / mblocks.  The weights are an input, not a predecessor's
+    // output, so its first K blocks can be brought into L2 now; a wrong
+    // guess costs only idle bandwidth.
+    const GemmPhase& P0 = args.p[0];
+    const unsigned h = ld_relaxed_gpu(args.spec_hint);
+    const bool wide = (h & 0xffff0000u) == kSpecHintTag &&
+                      static_cast<int>(h & 0xffffu) >= args.spec_min;
+    const int e = static_cast<int>(blockIdx.x) / P0.mblocks;
+    if (wide && e < args.spec_experts) {
+      const int a_row = e * P0.a_rows_per_e + (static_cast<int>(blockIdx.x) % P0.mblocks) * P0.row_step;
+      const int nk = P0.kblocks < 16 ? P0.kblocks : 16;
+      for (int kb = 0; kb < nk; ++kb) {
+        tma_prefetch_2d(&maps1.a, kb * BKE, a_row);
+        tma_prefetch_2d(&maps1.a, kb * BKE, a_row + P0.a_up_off);
+      }
+    }
+  };
+  // A launch whose kernel family the scan picks on the device waits for its
+  // predecessors first and leaves at once when the other family was picked,
+  // holding no TMEM and touching no barrier.
+  if (args.family) {
+    early_prefetch();
+    pdl_wait();
+    if (*args.family != args.family_want) return;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
@@ -174,36 +205,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (MODE != 2 && args.spec_hint && warp == 0 && lane == 0) {
-    // The routing, scan and gather kernels are still running and HBM is
-    // mostly idle.  With about one tile per expert in expert order (routing
-    // that touches nearly every expert, judged by the previous call), this
-    // CTA's first work item is likely item blockIdx.x: expert
-    // blockIdx.x / mblocks.  The weights are an input, not a predecessor's
-    // output, so its first K blocks can be brought into L2 now; a wrong
-    // guess costs only idle bandwidth.
-    const GemmPhase& P0 = args.p[0];
-    const unsigned h = ld_relaxed_gpu(args.spec_hint);
-    const bool wide = (h & 0xffff0000u) == kSpecHintTag &&
-                      static_cast<int>(h & 0xffffu) >= args.spec_min;
-    const int e = static_cast<int>(blockIdx.x) / P0.mblocks;
-    if (wide && e < args.spec_experts) {
-      const int a_row = e * P0.a_rows_per_e + (static_cast<int>(blockIdx.x) % P0.mblocks) * P0.row_step;
-      const int nk = P0.kblocks < 16 ? P0.kblocks : 16;
-      for (int kb = 0; kb < nk; ++kb) {
-        tma_prefetch_2d(&maps1.a, kb * BKE, a_row);
-        tma_prefetch_2d(&maps1.a, kb * BKE, a_row + P0.a_up_off);
-      }
-    }
-  }
   // everything above is local set-up; the tile lists and token rows are the
   // predecessor kernels' output
-  pdl_wait();
+  if (!args.family) {
+    early_prefetch();
+    pdl_wait();
+  }
 
-  // a device-chosen kernel family that is not this one: no work
-  const bool chosen = !args.family || *args.family == args.family_want;
-  const int nwork1 = (chosen && args.run1) ? (*args.p[0].ntiles) * args.p[0].mblocks : 0;
-  const int nwork2 = (chosen && args.run2) ? (*args.p[1].ntiles) * args.p[1].mblocks : 0;
+  const int nwork1 = args.run1 ? (*args.p[0].ntiles) * args.p[0].mblocks : 0;
+  const int nwork2 = args.run2 ? (*args.p[1].ntiles) * args.p[1].mblocks : 0;
   const int nwork = nwork1 + nwork2;
   int never = 0;
   bool ok = true;

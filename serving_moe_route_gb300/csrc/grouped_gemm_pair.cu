@@ -96,6 +96,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   float* cw = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [NM]
 
   pdl_trigger();
+  // A launch whose kernel family the scan picks on the device waits for its
+  // predecessors first and leaves at once (both CTAs read the same word)
+  // when the other family was picked, holding no TMEM and touching no
+  // barrier.
+  if (args.family) {
+    pdl_wait();
+    if (*args.family != args.family_want) return;
+  }
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);  // the even CTA's: its producer's arrival + bytes
@@ -123,11 +131,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   cluster_sync();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  pdl_wait();  // the tile list and token rows are the predecessor kernels' output
+  if (!args.family) pdl_wait();  // the tile list and token rows are the predecessors' output
 
-  // a device-chosen kernel family that is not this one: no work
-  const bool chosen = !args.family || *args.family == args.family_want;
-  const int nwork = chosen ? (*P.ntiles) * P.mblocks : 0;
+  const int nwork = (*P.ntiles) * P.mblocks;
   int never = 0;
   bool ok = true;
 

@@ -839,7 +839,7 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
   // BF16/F32 plans that run one CTA per tile and one fused launch, with
   // enough tokens for an expert to fill a 256-row CTA-pair tile, choose the
   // kernel family on the device, from the rows the experts actually hold
-  const bool dyn = !fp8 && !pair_plan && p->est <= 32 && NM1 == NM2 && T >= kHotRows;
+  const bool dyn = p->gemm_dyn != 0 && !fp8 && !pair_plan && p->est <= 32 && NM1 == NM2;
   unsigned* family = err + 2;
   launch_chained(scan_kernel, dim3(1), dim3(1024), 0, st, chunk_counts, p->n_chunks, EL, scan_tile,
                  per_expert, NM1, NM2, p->max_tiles, chunk_base, counts, offsets, tiles, ntiles,
@@ -1023,8 +1023,12 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
       return true;
     };
     if (dyn) {
-      // both families are enqueued; the one the scan did not choose finds
-      // no work.  Events: [4] after the single-CTA launch, [5] after the pair
+      // both families are enqueued; the launches of the one the scan did not
+      // choose leave at once.  Each such launch still costs a few us in the
+      // chain (its CTAs take the SMs' shared memory before they can leave);
+      // single-CTA first measured faster on uniform routing and the same on
+      // concentrated routing.  Events: [4] after the single-CTA launch, [5]
+      // after the CTA-pair launches
       if (!run_single(kFamilySingle, false)) return MOE_ERR_CUDA;
       mark(4);
       if (!run_pair(kFamilyPair, false)) return MOE_ERR_CUDA;
@@ -1162,6 +1166,9 @@ int moe_plan_ep(int T, int H, int I, int E, int k, int dtype, int scoring, int r
   p.gemm_pair = (dtype != MOE_DTYPE_FP8_BLOCK128 && p.est > 32) ? 1 : 0;
   // FP8 with 32 or more rows per expert on average: token-major GEMMs
   p.gemm_tm = (dtype == MOE_DTYPE_FP8_BLOCK128 && p.est >= kTmMinEst) ? 1 : 0;
+  // one-CTA-per-tile BF16/F32 plans whose batch can hold a whole 256-row
+  // CTA-pair tile for one expert: the device picks the family per call
+  p.gemm_dyn = (dtype != MOE_DTYPE_FP8_BLOCK128 && !p.gemm_pair && T >= kHotRows) ? 1 : 0;
   *plan = p;
   return MOE_OK;
 }
@@ -1178,7 +1185,9 @@ int moe_plan_describe(const moe_plan_t* p, char* buf, size_t n) {
       p->scoring ? "sigmoid" : "softmax", p->renorm,
       p->est, p->force_est ? " (forced)" : "", p->tile_n,
       (p->dtype == MOE_DTYPE_FP8_BLOCK128 && p->gemm_tm) ? "token-major"
-      : (p->dtype != MOE_DTYPE_FP8_BLOCK128 && p->gemm_pair) ? "cta-pair" : "swap-ab",
+      : (p->dtype != MOE_DTYPE_FP8_BLOCK128 && p->gemm_pair) ? "cta-pair"
+      : (p->dtype != MOE_DTYPE_FP8_BLOCK128 && p->gemm_dyn) ? "swap-ab|cta-pair (per call)"
+                                                            : "swap-ab",
       p->route_tpc, p->n_chunks, p->max_tiles, p->g1_mblocks, p->g2_mblocks,
       static_cast<unsigned long long>(p->workspace_bytes));
   return len;

@@ -64,11 +64,9 @@ def run_gpu(wl, inp, layer=None):
     inter["tile_n"] = layer.plan(wl.T).tile_n
     inter["gemm_pair"] = layer.plan(wl.T).gemm_pair
     inter["gemm_tm"] = layer.plan(wl.T).gemm_tm
-    # plans that pick the GEMM kernel family on the device (BF16/F32, est <= 32,
-    # T >= 256): an expert with 256 or more rows selects CTA pairs
-    plan = layer.plan(wl.T)
-    inter["dyn_family"] = (wl.dtype != W.FP8 and not plan.gemm_pair and plan.est <= 32
-                           and wl.T >= 256)
+    # plans that pick the GEMM kernel family on the device: an expert with 256
+    # or more rows selects CTA pairs
+    inter["dyn_family"] = bool(layer.plan(wl.T).gemm_dyn)
     inter["est"] = layer.plan(wl.T).est
     return out.float().cpu().double().numpy(), inter, layer
 

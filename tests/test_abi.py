@@ -179,3 +179,18 @@ def test_plan_gemm_tm_choice(B):
     assert B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).gemm_tm == 0
     assert "token-major" in B.moe_plan(4096, 2048, 768, 128, 8, fp8).describe()
     assert "cta-pair" in B.moe_plan(4096, 2048, 768, 128, 8, B.MOE_DTYPE_BF16).describe()
+
+
+def test_plan_gemm_dyn_choice(B):
+    # the device picks the GEMM kernel family for one-CTA-per-tile BF16/F32
+    # plans whose batch can give one expert a whole 256-row tile
+    bf16, f32, fp8 = B.MOE_DTYPE_BF16, B.MOE_DTYPE_F32, B.MOE_DTYPE_FP8_BLOCK128
+    assert B.moe_plan(288, 2048, 768, 400, 6, bf16).gemm_dyn == 1     # est 5
+    assert B.moe_plan(256, 256, 256, 128, 8, f32).gemm_dyn == 1       # est 16
+    assert B.moe_plan(255, 2048, 768, 400, 6, bf16).gemm_dyn == 0     # T < 256
+    assert B.moe_plan(128, 2048, 768, 128, 8, bf16).gemm_dyn == 0     # decode
+    p = B.moe_plan(4096, 2048, 768, 128, 8, bf16)                     # est 256: CTA pairs
+    assert p.gemm_pair == 1 and p.gemm_dyn == 0
+    assert B.moe_plan(288, 2048, 768, 400, 6, fp8).gemm_dyn == 0
+    assert "per call" in B.moe_plan(288, 2048, 768, 400, 6, bf16).describe()
+    assert "per call" not in B.moe_plan(128, 2048, 768, 128, 8, bf16).describe()
