@@ -288,10 +288,16 @@ __device__ __forceinline__ int expert_tile(int cnt, int tile_n, int per_expert, 
 // With heavy_first, the experts that fill at least one whole tile come
 // first (in expert order), then the rest: a grid-stride walk over the list
 // then deals the long items out evenly before the short ones.
+// An expert that needs several tiles has its rows split evenly over them
+// (rounded up to 16; at most the width): a tile's MMAs take time in
+// proportion to its rows above a floor (about N/2 cycles for N > 92 per
+// 128-row MMA), so 288 rows as 144 + 144 finish well before 256 + 32 would,
+// with the same weight traffic.
 __device__ void write_tile_list(int e, int E, int cnt, int off, int ne, int max_tiles,
                                bool heavy_first, int* warp_sums, int* tot, int4* tiles,
                                int* ntiles, unsigned* err) {
   const int ntl = (cnt + ne - 1) / ne;
+  const int step = ntl > 1 ? min(ne, (((cnt + ntl - 1) / ntl) + 15) & ~15) : ne;
   int tstart;
   if (heavy_first) {
     const bool heavy = cnt >= ne;
@@ -310,7 +316,7 @@ __device__ void write_tile_list(int e, int E, int cnt, int off, int ne, int max_
   }
   if (e < E)
     for (int i = 0; i < ntl && tstart + i < max_tiles; ++i)
-      tiles[tstart + i] = make_int4(e, off + i * ne, min(ne, cnt - i * ne), ne);
+      tiles[tstart + i] = make_int4(e, off + i * step, min(step, cnt - i * step), ne);
 }
 
 __global__ void __launch_bounds__(1024)

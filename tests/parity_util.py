@@ -150,6 +150,14 @@ def check_routing_and_permutation(wl, inp, inter):
             else:
                 want = min(n_max, max(tile_n, bucket))
             assert width == want, (key, e, c, width, want)
+            # an expert's rows are split evenly over ceil(c / width) tiles:
+            # every tile but the last holds `step` rows (the even share
+            # rounded up to 16, at most the width), in row order
+            ntl = -(-c // width)
+            step = width if ntl == 1 else min(width, -(-(-(-c // ntl)) // 16) * 16)
+            i = (r0 - offsets[e]) // step
+            assert r0 == offsets[e] + i * step and i < ntl, (key, e, c, r0, step)
+            assert n == min(step, c - i * step), (key, e, c, i, n, step)
             rows[e] += n
         np.testing.assert_array_equal(rows, counts)
     return ids_ref, w_ref
