@@ -12,7 +12,10 @@ namespace moe {
 
 constexpr unsigned kDevErrTimeout = 4u;
 constexpr int kEpiWarps = 8;  // two column halves per TMEM lane quadrant
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// warp 0 producer, warp 1 first MMA issuer, warps 2 .. 1 + kEpiWarps
+// epilogue, the last warp the second MMA issuer
+constexpr int kMmaWarp2 = 2 + kEpiWarps;
+constexpr int kThreads = 96 + 32 * kEpiWarps;
 
 template <int KIND>
 struct KindTraits;

@@ -171,19 +171,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 2);  // a commit from each MMA issuer
     }
     // epilogue-side barriers take one arrival per epilogue warp (lane 0,
     // after __syncwarp orders the warp's TMEM loads and shared stores)
     for (int b = 0; b < NS; ++b) {
-      mbar_init(smem_u32(&accf[b]), 1);
+      mbar_init(smem_u32(&accf[b]), 2);
       mbar_init(smem_u32(&acce[b]), kEpiWarps);
     }
-    mbar_init(smem_u32(done), 1);
+    mbar_init(smem_u32(done), 2);
     mbar_init(smem_u32(epib), kEpiWarps);
     for (int i = 0; i < kQueue; ++i) {
       mbar_init(smem_u32(&qfull[i]), 1);
-      mbar_init(smem_u32(&qempty[i]), 1 + kEpiWarps);
+      mbar_init(smem_u32(&qempty[i]), 2 + kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -291,8 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait(smem_u32(&full[j % S]), (j / S) & 1u, limit, &never);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == kMmaWarp2) {
+    // ------------------------------------------------------------ MMA issuers
+    // Two threads in different warps issue the MMAs of each K block: the
+    // first those of weight tile 0 (GEMM1 gate rows), the second those of
+    // tile 1 (up rows, or GEMM2's second 128 output rows).  At small N an
+    // MMA's issue cost on one thread, not the tensor pipe, sets the pace
+    // (about 110 cycles per MMA from one thread against 56 from two, for
+    // M=128, N<=64), so two issuers double the K blocks a CTA can consume.
+    // Both walk the same items and stages and both commit to every stage,
+    // accumulator and final barrier (each of which takes two arrivals).
+    const int my_a = warp == 1 ? 0 : 1;
     if (lane == 0) {
       uint32_t it = 0, tc = 0, gc = 0, qi = 0;
       int w_static = static_cast<int>(blockIdx.x);
@@ -355,7 +364,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t bd0 = sdesc_sw128(sa + NAM * 16384);
 #pragma unroll
           for (int a = 0; a < 2; ++a) {
-            if (a < na) {
+            if (a < na && a == my_a) {
               const uint64_t ad0 = sdesc_sw128(sa + a * 16384);
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks) {
