@@ -105,7 +105,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int S = args.stages;
   const int NS = args.nslots;
-  const int GS = FP8 ? (NS >> 1) : 1;  // FP8: K blocks per handed-over group
+  // FP8: the slots are handed between the MMAs and the epilogue in NG groups
+  // of GS K blocks (four groups once there are 8 slots or more, so that the
+  // epilogue frees slots often enough for the MMAs not to wait on it)
+  const uint32_t ng_shift = (FP8 && NS >= 8) ? 2u : 1u;
+  const uint32_t NG = 1u << ng_shift;
+  const int GS = FP8 ? (NS >> ng_shift) : 1;  // FP8: K blocks per handed-over group
   const int NM = args.n_max;
   const int NAM = args.na_max;
   const uint32_t stage_bytes = NAM * 16384u + static_cast<uint32_t>(NM) * 128u;
@@ -345,8 +350,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kb = 0; kb < kbs; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (FP8 && kb % GS == 0) {  // a new group of K blocks: its slots must be drained
-            buf = gc & 1u;
-            if (!mbar_wait(smem_u32(&acce[buf]), ((gc >> 1) & 1u) ^ 1u, limit, abort_flag)) {
+            buf = gc & (NG - 1u);
+            if (!mbar_wait(smem_u32(&acce[buf]), ((gc >> ng_shift) & 1u) ^ 1u, limit, abort_flag)) {
               ok = false;
               break;
             }
@@ -550,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc1[c] = 0.0f;
         }
         for (int kb0 = 0; kb0 < kbs; kb0 += GS, ++gc) {
-          const uint32_t buf = gc & 1u;
-          const bool got = mbar_wait(smem_u32(&accf[buf]), (gc >> 1) & 1u, limit, abort_flag);
+          const uint32_t buf = gc & (NG - 1u);
+          const bool got = mbar_wait(smem_u32(&accf[buf]), (gc >> ng_shift) & 1u, limit, abort_flag);
           if (!__all_sync(0xffffffffu, got)) {
             ok = false;
             break;
