@@ -51,7 +51,10 @@ __device__ __forceinline__ int half_map_index(int h) {
 // MMAs wait for the drain, so it is spread over more warps than in the
 // single-CTA kernel
 constexpr int kPairEpiWarps = 16;
-constexpr int kPairThreads = 64 + 32 * kPairEpiWarps;
+// warp 0 producer, warp 1 first MMA issuer, warps 2 .. 17 epilogue, the last
+// warp the second MMA issuer (GEMM1 up rows)
+constexpr int kPairMmaWarp2 = 2 + kPairEpiWarps;
+constexpr int kPairThreads = 96 + 32 * kPairEpiWarps;
 
 template <int KIND, int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
@@ -107,13 +110,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(smem_u32(&full[s]), 1);  // the even CTA's: its producer's arrival + bytes
-      mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 2);  // a commit from each MMA issuer
     }
     for (int b = 0; b < NS; ++b) {
-      mbar_init(smem_u32(&accf[b]), 1);
+      mbar_init(smem_u32(&accf[b]), 2);
       mbar_init(smem_u32(&acce[b]), 2 * EW);
     }
-    mbar_init(smem_u32(done), 1);
+    mbar_init(smem_u32(done), 2);
     mbar_init(smem_u32(epib), EW);
     *abort_flag = 0;
     fence_mbar_init();
@@ -187,8 +190,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         mbar_wait(smem_u32(&empty[j % S]), (j / S) & 1u, limit, &never);
     }
     __syncwarp();
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer (even CTA)
+  } else if (warp == 1 || warp == kPairMmaWarp2) {
+    // ------------------------------------------------------------ MMA issuers (even CTA)
+    // GEMM1's gate and up MMAs come from two threads in different warps
+    // (separate accumulators): below N = 256 a pair MMA's issue cost on one
+    // thread exceeds its tensor time.  GEMM2's MMAs all accumulate into one
+    // slot and stay on the first issuer, so that their order (and rounding)
+    // is fixed; the second issuer still commits to every barrier, each of
+    // which takes two arrivals.
+    const int my_a = warp == 1 ? 0 : 1;
     if (lane == 0 && leader) {
       uint32_t it = 0, tc = 0;
       int4 next = cid < nwork ? P.tiles[cid / P.mblocks] : int4{0, 0, 0, 0};
@@ -218,6 +228,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             const uint64_t bd0 = sdesc_sw128(sk + NA * 16384u);
 #pragma unroll
             for (int a = 0; a < NA; ++a) {
+              if (a != my_a) continue;
               const uint64_t ad0 = sdesc_sw128(sk + a * 16384u);
 #pragma unroll
               for (int ks = 0; ks < 4; ++ks)
