@@ -669,14 +669,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       if (MODE == 3 && I.g == 0) {
         // publish this GEMM1 item: all epilogue threads' activation stores
-        // become visible (to generic and TMA readers) before the count moves
+        // become visible (to generic and TMA readers) before the count moves.
+        // Each thread orders its stores for the async proxy; the barrier
+        // (mbarrier arrive/wait: release/acquire at CTA scope) orders them
+        // before the publishing thread, whose GPU-scope fence is cumulative
+        // over them -- one fence per item instead of one per thread.
         fence_proxy_async_global();
-        __threadfence();
         if (!ep_barrier()) {
           ok = false;
           break;
         }
-        if (ew == 0 && lane == 0) atomicAdd(args.dep + I.t, 1);
+        if (ew == 0 && lane == 0) {
+          __threadfence();
+          atomicAdd(args.dep + I.t, 1);
+        }
       }
     }
     if (!ok) {
