@@ -71,3 +71,34 @@ def test_every_benchmarked_workload_is_a_named_workload():
     # so nothing the sweep times goes without a parity test
     assert set(bench.SWEEP) <= set(W.workloads())
     assert "decode_bf16" in bench.SWEEP
+
+
+class _Plan:
+    def __init__(self, gemm_pair=0, gemm_tm=0, gemm_dyn=0):
+        self.gemm_pair, self.gemm_tm, self.gemm_dyn = gemm_pair, gemm_tm, gemm_dyn
+
+
+def test_gemm_roofline_attributes_the_launch_that_ran():
+    # stage times in ms; acc: GEMM1 and GEMM2 algorithmic bytes and FLOPs
+    pk = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "measured"}
+    acc = {"g1_bytes": 600e6, "g2_bytes": 300e6, "flops": 3e9}
+    wl = W.workloads()["sparse_concentrated_bf16"]
+    # a per-call plan that picked CTA pairs: the single-CTA launch (stage
+    # 'gemm1') returned at once, both GEMMs ran in stage 'gemm2'
+    st = {"gemm1": [0.006], "gemm2": [0.043]}
+    name, r = bench.gemm_roofline(wl, st, acc, pk, family=2, plan=_Plan(gemm_dyn=1))
+    assert "CTA pairs" in name and r["kernel"].startswith("moe_gemm_pair_kernel")
+    assert r["mean_ms"] == 0.043 and r["algorithmic_bytes"] == int(900e6)
+    # the same plan when the one-CTA-per-tile family ran (fused, stage 'gemm1')
+    st = {"gemm1": [0.55], "gemm2": [0.008]}
+    name, r = bench.gemm_roofline(wl, st, acc, pk, family=1, plan=_Plan(gemm_dyn=1))
+    assert "fused" in name and r["kernel"].startswith("moe_gemm_kernel")
+    assert r["mean_ms"] == 0.55
+    # plans that fix the family: the fused launch is recognised by an empty GEMM2 stage
+    name, r = bench.gemm_roofline(wl, st, acc, pk, family=None, plan=_Plan())
+    assert name == "gemm1+gemm2 fused"
+    # FP8 token-major plans name their kernel
+    wl8 = W.workloads()["fp8_T4096"]
+    st = {"gemm1": [0.176], "gemm2": [0.117]}
+    name, r = bench.gemm_roofline(wl8, st, acc, pk, family=None, plan=_Plan(gemm_tm=1))
+    assert name == "gemm1" and r["kernel"].startswith("moe_gemm_tm_kernel")
