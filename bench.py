@@ -460,7 +460,7 @@ def gemm_roofline(wl, stage_ms, acc, pk, family=None, plan=None):
 
 
 def layer_roofline(wl, step_ms, acc, pk):
-    """North-star roofline of the whole layer: max(FLOPs / tensor peak,
+    """Roofline of the whole layer: max(FLOPs / tensor peak,
     bytes / 8 TB/s); also against the measured copy bandwidth."""
     tp, _ = tensor_peak(wl, pk)
     t_c = acc["flops"] / (tp * 1e12)
