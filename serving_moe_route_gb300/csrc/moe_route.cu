@@ -68,6 +68,159 @@ __device__ __forceinline__ float load_logit(const __nv_bfloat16* p) {
   return __bfloat162float(p[0]);
 }
 
+// Values per logits load in routing: as many of a lane's VPT values as fit
+// 16 bytes (1: one logit per load)
+template <int VPT, typename LT>
+__host__ __device__ constexpr int vec_width() {
+  return (16 / static_cast<int>(sizeof(LT))) < VPT ? 16 / static_cast<int>(sizeof(LT)) : VPT;
+}
+
+// W consecutive logits of row t from expert e0 (the address aligned to W
+// elements), as floats
+template <typename LT, int W>
+__device__ __forceinline__ void load_logits(const LT* __restrict__ row, int e0, float (&out)[W]) {
+  if constexpr (W == 1) {
+    out[0] = load_logit(row + e0);
+  } else if constexpr (sizeof(LT) == 4) {  // f32: W in {2, 4}
+    if constexpr (W == 4) {
+      const float4 a = __ldg(reinterpret_cast<const float4*>(row + e0));
+      out[0] = a.x; out[1] = a.y; out[2] = a.z; out[3] = a.w;
+    } else {
+      const float2 a = __ldg(reinterpret_cast<const float2*>(row + e0));
+      out[0] = a.x; out[1] = a.y;
+    }
+  } else {  // bf16: W in {2, 4, 8}
+    uint32_t raw[W / 2];
+    if constexpr (W == 8) {
+      const uint4 a = __ldg(reinterpret_cast<const uint4*>(row + e0));
+      raw[0] = a.x; raw[1] = a.y; raw[2] = a.z; raw[3] = a.w;
+    } else if constexpr (W == 4) {
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(row + e0));
+      raw[0] = a.x; raw[1] = a.y;
+    } else {
+      raw[0] = __ldg(reinterpret_cast<const unsigned int*>(row + e0));
+    }
+#pragma unroll
+    for (int j = 0; j < W / 2; ++j) {
+      out[2 * j] = __uint_as_float(raw[j] << 16);              // low half: the lower expert
+      out[2 * j + 1] = __uint_as_float(raw[j] & 0xffff0000u);  // high half
+    }
+  }
+}
+
+// One token's routing by one warp (a-1): sanitised logits of token t, an
+// optional group mask, k rounds of warp arg-max (ties to the lower expert
+// index), then softmax or sigmoid weights, renormalised when asked.  Lanes
+// j < k end with pick j's expert (my_id) and weight (my_w).  Lane `lane`
+// holds value i of expert (i / W) * 32W + lane * W + i % W: its experts
+// ascend with i, and W consecutive experts come from one load.
+template <int VPT, typename LT, int W>
+__device__ __forceinline__ void route_token(const LT* __restrict__ logits, int t, int E, int k,
+                                            int scoring, int renorm, int n_group, int topk_group,
+                                            int lane, int& my_id, float& my_w) {
+  auto expert = [&](int i) { return (i / W) * 32 * W + lane * W + i % W; };
+  const LT* row = logits + static_cast<size_t>(t) * E;
+  float v[VPT];
+#pragma unroll
+  for (int b = 0; b < VPT / W; ++b) {
+    const int e0 = b * 32 * W + lane * W;
+    float part[W];
+    if (e0 < E) {  // with W > 1, E is a multiple of W: the whole load is in the row
+      load_logits<LT, W>(row, e0, part);
+    } else {
+#pragma unroll
+      for (int j = 0; j < W; ++j) part[j] = 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < W; ++j) v[b * W + j] = sanitize_logit(part[j]);
+  }
+  uint32_t vk[VPT];  // the logits' order keys (0: no expert in this slot)
+#pragma unroll
+  for (int i = 0; i < VPT; ++i) vk[i] = (expert(i) < E) ? logit_key(v[i]) : 0u;
+  uint32_t taken = 0;
+  if (n_group > 1) {
+    // group-limited routing: lane g holds the key of the largest sanitised
+    // logit of group g; keep the topk_group best groups (ties to the lower
+    // group) and exclude the other groups' experts below
+    const int gs = E / n_group;
+    uint32_t my_gkey = 0;
+    for (int g = 0; g < n_group; ++g) {
+      uint32_t m = 0;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        const int e = expert(i);
+        if (e < E && e / gs == g) m = max(m, vk[i]);
+      }
+      m = __reduce_max_sync(0xffffffffu, m);
+      if (lane == g) my_gkey = m;
+    }
+    uint32_t kept = 0;
+    bool mine_kept = false;
+    for (int r = 0; r < topk_group; ++r) {
+      const uint32_t ck = (lane < n_group && !mine_kept) ? my_gkey : 0u;
+      const uint32_t kmax = __reduce_max_sync(0xffffffffu, ck);
+      const uint32_t g = __reduce_min_sync(0xffffffffu, (ck == kmax) ? lane : 0xffffffffu);
+      kept |= 1u << g;
+      if (lane == static_cast<int>(g)) mine_kept = true;
+    }
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int e = expert(i);
+      if (e < E && !((kept >> (e / gs)) & 1u)) taken |= 1u << i;
+    }
+  }
+  float my_v = 0.0f;
+  for (int j = 0; j < k; ++j) {
+    // this lane's best remaining expert (lane-local experts ascend with i,
+    // so '>' keeps the lower index on ties), then the warp's: the largest
+    // key, and among lanes holding it the lowest expert index
+    uint32_t bk = 0;
+    uint32_t bi = 0xffffffffu;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      if (!((taken >> i) & 1u) && vk[i] > bk) {
+        bk = vk[i];
+        bi = static_cast<uint32_t>(expert(i));
+      }
+    }
+    const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t best = __reduce_min_sync(0xffffffffu, (bk == kmax) ? bi : 0xffffffffu);
+    // the winner's lane and its slot in that lane
+    const uint32_t wl = (best / W) % 32u, wi = (best / (32u * W)) * W + best % W;
+    if (wl == static_cast<uint32_t>(lane)) taken |= 1u << wi;
+    if (lane == j) {
+      my_id = static_cast<int>(best);
+      my_v = key_logit(kmax);
+    }
+  }
+  // weights
+  const float vmax = __shfl_sync(0xffffffffu, my_v, 0);  // pick 0 is the row maximum
+  float score = 0.0f;
+  if (scoring == 0) {
+    if (renorm) {
+      score = (lane < k) ? expf(my_v - vmax) : 0.0f;  // the full-row sum cancels
+    } else {
+      float z = 0.0f;
+#pragma unroll
+      for (int i = 0; i < VPT; ++i)
+        if (expert(i) < E) z += expf(v[i] - vmax);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      score = (lane < k) ? expf(my_v - vmax) / z : 0.0f;
+    }
+  } else {
+    score = (lane < k) ? 1.0f / (1.0f + expf(-my_v)) : 0.0f;
+  }
+  if (renorm) {
+    float den = score;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+    my_w = (den > 0.0f && isfinite(den)) ? score / den : 1.0f / static_cast<float>(k);
+  } else {
+    my_w = score;
+  }
+}
+
 // mode 0: routing only; 1: routing + histogram; 2: validate caller ids + histogram
 template <int VPT, typename LT>
 __global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
@@ -89,95 +242,18 @@ __global__ void __launch_bounds__(VPT <= 8 ? 1024 : kRouteThreads, 1)
     int my_id = -1;
     float my_w = 0.0f;
     if (mode != 2) {
-      float v[VPT];
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) {
-        const int e = i * 32 + lane;
-        v[i] = (e < E) ? sanitize_logit(load_logit(logits + static_cast<size_t>(t) * E + e)) : 0.0f;
-      }
-      uint32_t vk[VPT];  // the logits' order keys (0: no expert in this slot)
-#pragma unroll
-      for (int i = 0; i < VPT; ++i) vk[i] = (i * 32 + lane < E) ? logit_key(v[i]) : 0u;
-      uint32_t taken = 0;
-      if (n_group > 1) {
-        // group-limited routing: lane g holds the key of the largest
-        // sanitised logit of group g; keep the topk_group best groups (ties
-        // to the lower group) and exclude the other groups' experts below
-        const int gs = E / n_group;
-        uint32_t my_gkey = 0;
-        for (int g = 0; g < n_group; ++g) {
-          uint32_t m = 0;
-#pragma unroll
-          for (int i = 0; i < VPT; ++i) {
-            const int e = i * 32 + lane;
-            if (e < E && e / gs == g) m = max(m, vk[i]);
-          }
-          m = __reduce_max_sync(0xffffffffu, m);
-          if (lane == g) my_gkey = m;
-        }
-        uint32_t kept = 0;
-        bool mine_kept = false;
-        for (int r = 0; r < topk_group; ++r) {
-          const uint32_t ck = (lane < n_group && !mine_kept) ? my_gkey : 0u;
-          const uint32_t kmax = __reduce_max_sync(0xffffffffu, ck);
-          const uint32_t g = __reduce_min_sync(0xffffffffu, (ck == kmax) ? lane : 0xffffffffu);
-          kept |= 1u << g;
-          if (lane == static_cast<int>(g)) mine_kept = true;
-        }
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          const int e = i * 32 + lane;
-          if (e < E && !((kept >> (e / gs)) & 1u)) taken |= 1u << i;
-        }
-      }
-      float my_v = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        // this lane's best remaining expert (lane-local experts ascend with
-        // i, so '>' keeps the lower index on ties), then the warp's: the
-        // largest key, and among lanes holding it the lowest expert index
-        uint32_t bk = 0;
-        uint32_t bi = 0xffffffffu;
-#pragma unroll
-        for (int i = 0; i < VPT; ++i) {
-          if (!((taken >> i) & 1u) && vk[i] > bk) {
-            bk = vk[i];
-            bi = static_cast<uint32_t>(i * 32 + lane);
-          }
-        }
-        const uint32_t kmax = __reduce_max_sync(0xffffffffu, bk);
-        const uint32_t best = __reduce_min_sync(0xffffffffu, (bk == kmax) ? bi : 0xffffffffu);
-        if ((best & 31u) == static_cast<uint32_t>(lane)) taken |= 1u << (best >> 5);
-        if (lane == j) {
-          my_id = static_cast<int>(best);
-          my_v = key_logit(kmax);
-        }
-      }
-      // weights
-      const float vmax = __shfl_sync(0xffffffffu, my_v, 0);  // pick 0 is the row maximum
-      float score = 0.0f;
-      if (scoring == 0) {
-        if (renorm) {
-          score = (lane < k) ? expf(my_v - vmax) : 0.0f;  // the full-row sum cancels
-        } else {
-          float z = 0.0f;
-#pragma unroll
-          for (int i = 0; i < VPT; ++i)
-            if (i * 32 + lane < E) z += expf(v[i] - vmax);
-#pragma unroll
-          for (int off = 16; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
-          score = (lane < k) ? expf(my_v - vmax) / z : 0.0f;
-        }
-      } else {
-        score = (lane < k) ? 1.0f / (1.0f + expf(-my_v)) : 0.0f;
-      }
-      if (renorm) {
-        float den = score;
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
-        my_w = (den > 0.0f && isfinite(den)) ? score / den : 1.0f / static_cast<float>(k);
-      } else {
-        my_w = score;
-      }
+      // logits read W to a load when the row length and the pointer allow
+      // it (W consecutive experts per lane per load), else one per load;
+      // the picks are the same either way
+      constexpr int WV = vec_width<VPT, LT>();
+      const bool vec = WV > 1 && E % WV == 0 &&
+                       (reinterpret_cast<uintptr_t>(logits) % (WV * sizeof(LT))) == 0;
+      if (vec)
+        route_token<VPT, LT, WV>(logits, t, E, k, scoring, renorm, n_group, topk_group, lane,
+                                 my_id, my_w);
+      else
+        route_token<VPT, LT, 1>(logits, t, E, k, scoring, renorm, n_group, topk_group, lane,
+                                my_id, my_w);
     } else {
       // caller-supplied picks: an id outside [0, E) or repeated within the
       // token is reported and skipped rather than used as an index
