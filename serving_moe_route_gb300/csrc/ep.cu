@@ -132,7 +132,16 @@ __global__ void __launch_bounds__(256)
   const int t = send_tokens[row];
   const XT* src = x + static_cast<size_t>(t) * H;
   XT* dst = x_send + static_cast<size_t>(row) * H;
-  for (int h = lane; h < H; h += 32) dst[h] = src[h];
+  // 16 bytes per lane and step when the rows allow it, else one element
+  constexpr int VW = 16 / static_cast<int>(sizeof(XT));
+  if (H % VW == 0 && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(x_send) & 15) == 0) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+    for (int h = lane; h < H / VW; h += 32) d4[h] = s4[h];
+  } else {
+    for (int h = lane; h < H; h += 32) dst[h] = src[h];
+  }
   if (lane < k) {
     ids_send[static_cast<size_t>(row) * k + lane] = ids[static_cast<size_t>(t) * k + lane];
     w_send[static_cast<size_t>(row) * k + lane] = w[static_cast<size_t>(t) * k + lane];
@@ -151,17 +160,33 @@ __global__ void __launch_bounds__(256)
   const int h0 = static_cast<int>(g % chunks) * 256 + lane * 8;
   const int my_row = lane < ep_size ? row_of[static_cast<size_t>(t) * ep_size + lane] : -1;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  // two 16-byte loads per row when this lane's 8 columns are whole and aligned
+  const bool vec = h0 + 8 <= H && (H & 3) == 0 && (reinterpret_cast<uintptr_t>(back) & 15) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out) & 15) == 0;
   for (int d = 0; d < ep_size; ++d) {
     const int r = __shfl_sync(0xffffffffu, my_row, d);
     if (r < 0) continue;
     const float* p = back + static_cast<size_t>(r) * H + h0;
+    if (vec) {
+      const float4 a = reinterpret_cast<const float4*>(p)[0];
+      const float4 b = reinterpret_cast<const float4*>(p)[1];
+      acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+      acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (h0 + i < H) acc[i] += p[i];
+    }
+  }
+  if (vec) {
+    float4* o = reinterpret_cast<float4*>(out + static_cast<size_t>(t) * H + h0);
+    o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (h0 + i < H) acc[i] += p[i];
+      if (h0 + i < H) out[static_cast<size_t>(t) * H + h0 + i] = acc[i];
   }
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if (h0 + i < H) out[static_cast<size_t>(t) * H + h0 + i] = acc[i];
 }
 
 }  // namespace moe
