@@ -43,7 +43,7 @@ def test_route_workloads(name, renorm):
 
 @pytest.mark.parametrize("scoring", [0, 1])
 @pytest.mark.parametrize("E,k", [(8, 2), (40, 3), (128, 8), (400, 6), (1024, 32), (33, 32),
-                                 (1, 1), (64, 1)])
+                                 (1, 1), (64, 1), (250, 6), (260, 6)])
 def test_route_edge_rows(E, k, scoring):
     g = torch.Generator().manual_seed(E * 100 + k)
     T = 70
@@ -66,6 +66,25 @@ def test_route_edge_rows(E, k, scoring):
         ids = _compare(lg.to(dt), k, scoring, True)
         assert list(ids[0]) == list(range(k))
         assert list(ids[1]) == list(range(k))
+
+
+def test_route_unaligned_logits_pointer():
+    # logits read several to a load need an aligned pointer; a view that
+    # starts one element into its buffer takes the one-per-load path and
+    # must pick the same experts
+    g = torch.Generator().manual_seed(11)
+    T, E, k = 40, 128, 8
+    lg = torch.randn(T, E, generator=g)
+    dev = torch.device("cuda", 0)
+    for dt in (torch.float32, torch.bfloat16):
+        buf = torch.empty(T * E + 1, dtype=dt, device=dev)
+        view = buf[1:].view(T, E)
+        view.copy_(lg.to(dt).to(dev))
+        assert view.data_ptr() % 16 != 0
+        ids_u, w_u = route_topk(view, k)
+        ids_ref, w_ref = oracle.route(lg.to(dt).float().numpy(), k)
+        np.testing.assert_array_equal(ids_u.cpu().numpy(), ids_ref)
+        np.testing.assert_allclose(w_u.cpu().numpy(), w_ref, rtol=0, atol=2e-6)
 
 
 def test_route_rejects_k_above_32():
