@@ -16,7 +16,10 @@
 // epilogue), so CTAs that run out of GEMM1 work start GEMM2 work at once.
 //
 //   warp 0      TMA producer: weight tile(s) + token tile per 128-byte K step
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer
+//   warp 1      TMEM allocator; tcgen05.mma issuer of weight tile 0
+//   warp 10     tcgen05.mma issuer of weight tile 1 (GEMM1 up rows, GEMM2's
+//               second 128 output rows): at small N one thread's issue cost
+//               sets the MMA rate, so the two tiles' MMAs come from two
 //   warps 2..9  epilogue: tcgen05.ld from TMEM, then
 //                 GEMM1: act = SiLU(gate) * up  (FP8: + per-token 128-group
 //                        e4m3 quantisation, clamp with fminf/fmaxf as in
@@ -26,9 +29,9 @@
 //                        kernel)
 //
 // FP8 [128,128] block scales (Lab notes #6, config file line): each 128-K
-// block is accumulated into its own TMEM slot; the slots form two groups
-// (up to 8 blocks each) handed between the MMA warp and the epilogue as a
-// unit, and the epilogue folds every block into fp32 registers with the
+// block is accumulated into its own TMEM slot; the slots form groups (four
+// once there are eight slots or more, else two) handed between the MMA
+// warps and the epilogue as a unit, and the epilogue folds every block into fp32 registers with the
 // product weight-scale x activation-scale, so arbitrary fp32 scales are
 // honoured.  FP8 kernels are specialised per tile width (16/32/64; the
 // gate and up register accumulators of a 128-wide tile would not fit).

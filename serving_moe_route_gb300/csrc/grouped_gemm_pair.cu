@@ -20,7 +20,11 @@
 //
 //   warp 0      TMA producer of this CTA's half of every stage; the copies
 //               of both CTAs complete on the even CTA's `full` barrier
-//   warp 1      TMEM allocation (both CTAs); MMA issue (even CTA only)
+//   warp 1      TMEM allocation (both CTAs); MMA issue (even CTA only):
+//               GEMM1's gate MMAs and all of GEMM2's
+//   warp 18     GEMM1's up MMAs (even CTA only; a second issuer, since one
+//               thread's issue cost exceeds a pair MMA's tensor time below
+//               N = 256)
 //   warps 2..17 epilogue of this CTA's 128 rows (four warps per TMEM lane
 //               quadrant, each a quarter of the token columns); the
 //               drained-slot signal goes to the even CTA's `acce` barrier
