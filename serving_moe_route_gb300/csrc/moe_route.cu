@@ -1106,11 +1106,13 @@ static int forward_impl(const moe_plan_t* p, const void* x, const void* logits, 
     };
     if (dyn) {
       // both families are enqueued; the launches of the one the scan did not
-      // choose leave at once.  Each such launch still costs a few us in the
-      // chain (its CTAs take the SMs' shared memory before they can leave);
-      // single-CTA first measured faster on uniform routing and the same on
-      // concentrated routing.  Events: [4] after the single-CTA launch, [5]
-      // after the CTA-pair launches
+      // choose leave right after their dependent-launch wait.  The chain
+      // still runs about 5 us longer than a plan that fixes the CTA-pair
+      // family; leaving before the wait (the next launch then waiting for
+      // the gather's CTAs itself), or setting up before it, measured no
+      // faster.  Single-CTA first measured faster on uniform routing and the
+      // same on concentrated routing.  Events: [4] after the single-CTA
+      // launch, [5] after the CTA-pair launches
       if (!run_single(kFamilySingle, false)) return MOE_ERR_CUDA;
       mark(4);
       if (!run_pair(kFamilyPair, false)) return MOE_ERR_CUDA;

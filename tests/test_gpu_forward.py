@@ -223,6 +223,56 @@ def test_forward_in_a_cuda_graph():
     assert rc == 0, bits
 
 
+def test_per_call_family_in_a_cuda_graph():
+    # a plan that picks the GEMM kernel family per call, captured once and
+    # replayed on inputs that alternate between concentrated routing (CTA
+    # pairs) and uniform routing (one CTA per tile), the launches of the
+    # family not picked returning at once.  Each input's eager output matches
+    # the oracle; every replay equals it bit for bit, so no replay reads
+    # permuted rows, tile lists or a family word left by the one before.
+    shape = dict(T=520, H=256, I=256, E=128, k=4, dtype=W.BF16)
+    kinds = [(72, "concentrated", 2), (73, "concentrated", 2), (74, "normal", 1)]
+    wl = W.custom("family_graph", seed=72, logits="concentrated", **shape)
+    inp = W.make_inputs(wl)
+    layer = PU.make_layer(wl, inp)
+    assert layer.plan(wl.T).gemm_dyn == 1
+    dev = layer.device
+    tokens = PU.all_tokens(wl)
+    acts = [W.make_activations(W.custom(seed=s, logits=lk, **shape)) for s, lk, _ in kinds]
+    eager = []
+    for a, (_, _, fam) in zip(acts, kinds):
+        o = layer.forward(a["x"].to(dev), a["logits"].to(dev)).clone()
+        rc, bits = layer.check(wl.T)
+        assert rc == 0, bits
+        assert int(layer.intermediates(wl.T)["family"][0]) == fam
+        full = dict(inp)
+        full.update(a)
+        ref, _, _ = PU.run_oracle(wl, full, tokens)
+        PU.check_outputs(wl, o.float().cpu().double().numpy(), ref, tokens)
+        eager.append(o)
+    x = acts[0]["x"].to(dev)
+    lg = acts[0]["logits"].to(dev)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        layer.forward(x, lg, out)
+    torch.cuda.current_stream().wait_stream(side)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        layer.forward(x, lg, out)
+    for i in range(24):
+        j = i % len(kinds)
+        x.copy_(acts[j]["x"])
+        lg.copy_(acts[j]["logits"])
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager[j]), (i, j)
+        assert int(layer.intermediates(wl.T)["family"][0]) == kinds[j][2]
+    rc, bits = layer.check(wl.T)
+    assert rc == 0, bits
+
+
 @pytest.mark.parametrize("dtype", [W.BF16, W.FP8])
 def test_expert_parallel_slices(dtype):
     # each expert-parallel rank computes its experts' share (ids global and
